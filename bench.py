@@ -1,0 +1,415 @@
+"""Benchmark: sparse top-k MLA decode on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smla|reference]
+                    [--workload decode|prefill|large_prefill] [--extra-lines]
+
+A step is one smla_forward call (index resolve, gather + FP8 dequant, QK^T, softmax with
+sink, PV, split-K partials, combine) over the decode workload: 64 sequences x 16384 cached
+tokens, T = 64 query tokens, H = 64 heads, top-k 2048 (5% masked), FP8 KV, per-head sink.
+Eight index sets (and query sets) rotate between steps so that every call gathers its rows
+from HBM (8 x 81.7 MB of distinct rows > the 129 MB L2); the cache itself is 688 MB.
+
+One JSON line is printed by rank 0. `value` is gathered-KV GB/s over all ranks; `e2e`
+repeats the measurement with the step's inputs copied from pinned host memory and the
+outputs copied back inside the timed region. `--impl reference` times the fp64 CPU oracle
+(the only other implementation this project has) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA prefill TFLOP/s & decode µs/call + GB/s, as % of roofline"
+ROTATIONS = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill"])
+    ap.add_argument("--extra-lines", action="store_true",
+                    help="also print one JSON line per secondary workload to stderr")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workloads
+def build_workloads(kind):
+    from sparse_top_mla_gb300 import synth
+    if kind == "decode":
+        base = synth.config(2)
+        rots = [base]
+        for r in range(1, ROTATIONS):
+            rng = np.random.default_rng(2000 + r)
+            idx = synth.mask_random(rng, synth.distinct_indices(rng, np.full(base.T, 16383), 2048), 0.05)
+            q = synth.make_q(rng, base.T, base.H)
+            rots.append(synth.replace(base, q=q, main=synth.replace(base.main, indices=idx)))
+        return rots, "decode fp8: 64 seqs x 16384 ctx (688 MB cache), T=64, H=64, topk=2048 (5% -1), sink"
+    if kind == "prefill":
+        return [synth.config(3)], "prefill bf16: 1 seq x 32768 ctx, T=4096, H=32, topk=512 causal, sink"
+    return [synth.config(4)], ("large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T=8192, H=128, "
+                               "topk=2048 causal + 128-token window, sink")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "of measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_top_mla_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_key):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
+    when the kernel sources changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(workload_key)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    from sparse_top_mla_gb300 import synth
+    oracle.build()
+    w = synth.config(2) if args.workload == "decode" else (synth.config(3) if args.workload == "prefill"
+                                                             else synth.config(4, T=64))
+    per_tok = w.gathered_bytes() / w.T
+    n_tok = {"decode": 64, "prefill": 256, "large_prefill": 16}[args.workload]
+    threads = oracle.threads(0)
+    times = []
+    for s in range(args.warmup + args.steps):
+        tok = (np.arange(n_tok) + s * n_tok) % w.T
+        t0 = time.perf_counter()
+        oracle.attention(w, tokens=tok, nthreads=threads)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    gbs = per_tok * n_tok * len(times) / total / 1e9
+    sample = f"{n_tok} query tokens of the workload per step (of {w.T}); fp64 oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- smla arm
+def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
+    import torch
+    from sparse_top_mla_gb300 import binding
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    rots, label = build_workloads(kind)
+    probs = [binding.DeviceProblem(rots[0], device=dev)]
+    # the other rotations share the first rotation's device cache (only q and indices differ)
+    for w in rots[1:]:
+        probs.append(binding.DeviceProblem(w, device=dev, share_caches_with=probs[0]))
+    for p in probs:
+        p.ensure_workspace()
+    w0 = rots[0]
+    gathered = [w.gathered_bytes() for w in rots]
+    flops = w0.flops()
+    idx_bytes = sum(w0.main.indices[:, :w0.main.topk].nbytes for _ in [0]) + (
+        w0.extra.indices[:, :w0.extra.topk].nbytes if w0.extra is not None else 0)
+    q_bytes = w0.T * w0.H * 576 * 2
+    stream = torch.cuda.current_stream()
+    # warm-up
+    for s in range(warmup):
+        binding.forward(probs[s % len(probs)].call, stream)
+    torch.cuda.synchronize()
+    assert binding.device_error() == 0
+    # timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in kev:  # torch creates CUDA events lazily: record once so the handles exist for the library
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(steps):
+        p = probs[s % len(probs)]
+        binding.set_timing_events(kev[s][0], kev[s][1])
+        ev[s][0].record(stream)
+        binding.forward(p.call, stream)
+        ev[s][1].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    binding.set_timing_events(None, None)
+    clk = clocks.stop()
+    assert binding.device_error() == 0
+    total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world)
+    kern_ms = [kev[s][0].elapsed_time(kev[s][1]) for s in range(steps)]
+    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(steps)]
+    bytes_steps = sum(gathered[s % len(probs)] for s in range(steps))
+    value = bytes_steps * world / (total_ms * 1e-3) / 1e9
+    # launches per step: attention kernel + combine when split-K is used
+    splits_used = probs[0].workspace is not None and binding.workspace_size(probs[0].call) > 0
+    decode_route = w0.T <= binding.decode_max_tokens(w0.H, w0.main.topk + (w0.extra.topk if w0.extra else 0),
+                                                      w0.main.fmt)
+    launches_per_step = 2 if (decode_route and splits_used) else 1
+
+    # e2e: pinned host inputs -> device, forward, outputs -> pinned host, every step
+    h_q = [torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory() for w in rots]
+    h_idx = [torch.from_numpy(np.ascontiguousarray(w.main.indices)).pin_memory() for w in rots]
+    h_meta = [torch.from_numpy(np.concatenate([w.token_seq, w.main.seq_lens, w.main.block_table.reshape(-1)]))
+              .pin_memory() for w in rots]
+    h_sink = [torch.from_numpy(w.sink).pin_memory() if w.sink is not None else None for w in rots]
+    h_out = torch.empty((w0.T, w0.H, 512), dtype=torch.int16).pin_memory()
+    h_lse = torch.empty((w0.T, w0.H), dtype=torch.float32).pin_memory()
+    h2d = h_q[0].numel() * 2 + h_idx[0].numel() * 4 + h_meta[0].numel() * 4 + (h_sink[0].numel() * 4 if h_sink[0]
+                                                                                 is not None else 0)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e_steps = min(steps, 20)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(e2e_steps):
+        r = s % len(probs)
+        p = probs[r]
+        p.q.view(torch.int16).copy_(h_q[r].view(p.q.shape), non_blocking=True)
+        p.main.indices.copy_(h_idx[r], non_blocking=True)
+        meta = h_meta[r]
+        T, S = w0.T, w0.num_seqs
+        p.token_seq.copy_(meta[:T], non_blocking=True)
+        p.main.seq_lens.copy_(meta[T:T + S], non_blocking=True)
+        p.main.block_table.view(-1).copy_(meta[T + S:], non_blocking=True)
+        if h_sink[r] is not None:
+            p.sink.copy_(h_sink[r], non_blocking=True)
+        binding.forward(p.call, stream)
+        h_out.copy_(p.out.view(torch.int16), non_blocking=True)
+        h_lse.copy_(p.lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = sum(gathered[s % len(probs)] for s in range(e2e_steps)) * world / (e2e_ms * 1e-3) / 1e9
+
+    peaks = measured_peaks()
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    res = {"label": label, "w0": w0, "value": value, "total_ms": total_ms, "steps": steps,
+           "ms_per_step": total_ms / steps, "kern_avg_ms": kern_avg_ms, "step_ms": step_ms,
+           "gathered": gathered[0], "flops": flops, "idx_bytes": idx_bytes, "q_bytes": q_bytes, "clocks": clk,
+           "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "steps": e2e_steps}, "launches": launches_per_step * steps, "peaks": peaks}
+    return res
+
+
+def cpu_baseline_decode():
+    import oracle
+    from sparse_top_mla_gb300 import synth
+    oracle.build()
+    w = synth.config(2)
+    threads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.attention(w, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": w.gathered_bytes() / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "the whole decode batch (64 tokens x 64 heads x 2048 entries), one pass, fp64 oracle",
+            "seconds": dt}
+
+
+def roofline_for(kind, r):
+    peaks = r["peaks"]
+    if kind == "decode":
+        alg = r["gathered"] + r["idx_bytes"] + r["q_bytes"]
+        achieved = alg / (r["kern_avg_ms"] * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("decode"),
+                "algorithmic_bytes_per_launch": alg, "kernel": "sparse_mla_kernel<64> (split-K partials)",
+                "peak_source": peaks["source"] + " (hbm_gbs, STREAM-style copy)"}
+    achieved = r["flops"] / (r["kern_avg_ms"] * 1e-3) / 1e12
+    pk = peaks["bf16_tflops"]
+    return {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+            "traffic": ncu_traffic(kind), "algorithmic_flops_per_launch": r["flops"],
+            "peak_source": peaks["source"] + " (bf16_tflops burst, cuBLAS)"}
+
+
+def line_for(kind, r, args, world, cpu):
+    w0 = r["w0"]
+    us = r["ms_per_step"] * 1e3
+    rl = roofline_for(kind, r)
+    d = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world, "steps": r["steps"],
+         "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+         "config": {"workload": r["label"], "l2": ("inputs larger than L2: 8 rotating index/query sets over a "
+                                                   "688 MB cache (654 MB of distinct gathered rows)")
+                    if kind == "decode" else "single input set; per-call reuse stays in L2 as in serving",
+                    "us_per_call": us, "tflops": r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12,
+                    "kernel_avg_us": r["kern_avg_ms"] * 1e3, "gathered_bytes_per_call": r["gathered"]},
+         "roofline": rl, "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": r["launches"]}
+    if cpu is not None:
+        d["cpu_baseline"] = cpu
+    return d
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+    from sparse_top_mla_gb300 import build as smla_build
+    if rank == 0:
+        smla_build.build()
+    barrier(world)
+    r = time_workload(args.workload, args.steps, args.warmup, world, rank, local, True)
+    cpu = cpu_baseline_decode() if (rank == 0 and world == 1 and args.workload == "decode") else None
+    if rank == 0:
+        print(json.dumps(line_for(args.workload, r, args, world, cpu)), flush=True)
+    if args.extra_lines:
+        for kind in ("prefill", "large_prefill"):
+            rr = time_workload(kind, max(3, args.steps // 5), args.warmup, world, rank, local, False)
+            if rank == 0:
+                print(json.dumps(line_for(kind, rr, args, world, None)), file=sys.stderr, flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

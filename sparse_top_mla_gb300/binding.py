@@ -222,18 +222,22 @@ def device_error() -> int:
 
 
 def set_timing_events(start=None, stop=None) -> None:
+    """Hand two recorded torch.cuda.Event objects to the library's measurement hook."""
     a = None if start is None else ctypes.c_void_p(start.cuda_event)
     b = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    if (start is not None and not a.value) or (stop is not None and not b.value):
+        raise ValueError("timing events must have been recorded once (torch creates them lazily)")
     _check(load().smla_set_timing_events(a, b), "smla_set_timing_events")
 
 
 # ---------------------------------------------------------------------------------------
 # host workload -> device tensors (byte copies only)
 # ---------------------------------------------------------------------------------------
-def upload_set(s, device) -> DeviceSet:
+def upload_set(s, device, cache=None) -> DeviceSet:
+    """Copy one set's arrays to the device (reusing `cache`, a device tensor, when given)."""
     import torch
     t = lambda a: torch.from_numpy(a).to(device)  # noqa: E731
-    return DeviceSet(t(s.cache), s.fmt, s.row_stride, s.page_stride, s.num_pages, t(s.block_table),
+    return DeviceSet(t(s.cache) if cache is None else cache, s.fmt, s.row_stride, s.page_stride, s.num_pages, t(s.block_table),
                      t(s.seq_lens), t(s.indices), s.topk, None if s.topk_length is None else t(s.topk_length))
 
 
@@ -241,7 +245,7 @@ class DeviceProblem:
     """A synth.Workload copied to one GPU, with output buffers and a ready Call."""
 
     def __init__(self, w, device="cuda", lse: bool = True, out_pad: int = 0, lse_pad: int = 0,
-                 q_pad: tuple = (0, 0)):
+                 q_pad: tuple = (0, 0), share_caches_with: "Optional[DeviceProblem]" = None):
         import numpy as np
         import torch
         self.w = w
@@ -252,8 +256,10 @@ class DeviceProblem:
         q_full[:, :w.H, :576] = torch.from_numpy(qc).to(self.device)
         self.q = q_full.view(torch.bfloat16)[:, :w.H, :576]
         self.token_seq = torch.from_numpy(np.ascontiguousarray(w.token_seq, dtype=np.int32)).to(self.device)
-        self.main = upload_set(w.main, self.device)
-        self.extra = upload_set(w.extra, self.device) if w.extra is not None else None
+        src = share_caches_with
+        self.main = upload_set(w.main, self.device, None if src is None else src.main.cache)
+        self.extra = (upload_set(w.extra, self.device, None if src is None or src.extra is None else src.extra.cache)
+                      if w.extra is not None else None)
         self.sink = torch.from_numpy(w.sink).to(self.device) if w.sink is not None else None
         self.out_full = torch.full((w.T, w.H, 512 + out_pad), float("nan"), dtype=torch.bfloat16, device=self.device)
         self.out = self.out_full[:, :, :512]

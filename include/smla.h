@@ -131,6 +131,19 @@ smla_status smla_prefill(const smla_params* p, smla_stream_t stream);
  * rows, KV-bandwidth-bound; flashinfer PR "explain ..." merged body: decode split-K.) */
 smla_status smla_decode(const smla_params* p, smla_stream_t stream);
 
+/* smla_decode without a caller-provided workspace. The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory themselves (a plugin behind a
+ * fixed C interface that passes only the problem tensors, or a runtime whose device memory
+ * is wholly owned by its own pool). It ignores p->workspace / p->workspace_bytes and keeps
+ * the split-K partials in a 32 MiB array inside the library, which every GPU that loads
+ * libsmla holds until the process exits; it calls no allocator. Problems whose
+ * smla_workspace_size() exceeds 32 MiB are rejected with SMLA_ERR_WORKSPACE before any
+ * launch. The first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture. All calls on a device
+ * share the one array: calls that overlap on the GPU (unordered streams) race, so order
+ * them. Results equal smla_decode's. */
+smla_status smla_decode_static(const smla_params* p, smla_stream_t stream);
+
 /* Calibrated dispatch (flashinfer PR "explain ..." merged body, Dispatch: crossover —
  * decode serves T <= decode_max_tokens for the configuration, prefill serves the rest).
  * Routes to smla_decode when T <= smla_decode_max_tokens(H, topk total, main format),

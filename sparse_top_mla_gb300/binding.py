@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(HERE, "libsmla.so")
 SMLA_OK, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE, SMLA_ERR_CUDA, SMLA_ERR_DEVICE = range(6)
 KV_BF16, KV_FP8 = 0, 1
 
-EXPORTS = ("smla_supported", "smla_workspace_size", "smla_prefill", "smla_decode", "smla_forward",
+EXPORTS = ("smla_supported", "smla_workspace_size", "smla_prefill", "smla_decode", "smla_decode_static",
+           "smla_forward",
            "smla_decode_max_tokens", "smla_set_crossover", "smla_load_crossover", "smla_status_string",
            "smla_device_error", "smla_set_timing_events", "smla_struct_size", "smla_version")
 
@@ -67,6 +68,7 @@ def load(path: Optional[str] = None):
         "smla_workspace_size": ([P], ctypes.c_size_t),
         "smla_prefill": ([P, vp], ctypes.c_int),
         "smla_decode": ([P, vp], ctypes.c_int),
+        "smla_decode_static": ([P, vp], ctypes.c_int),
         "smla_forward": ([P, vp], ctypes.c_int),
         "smla_decode_max_tokens": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
         "smla_set_crossover": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
@@ -189,6 +191,14 @@ def decode(call: Call, stream=None, check: bool = True) -> int:
     st = load().smla_decode(call.ref(), _stream(stream))
     if check:
         _check(st, "smla_decode", call)
+    return st
+
+
+def decode_static(call: Call, stream=None, check: bool = True) -> int:
+    """smla_decode_static: split-K decode with the library's own fixed scratch (no workspace)."""
+    st = load().smla_decode_static(call.ref(), _stream(stream))
+    if check:
+        _check(st, "smla_decode_static", call)
     return st
 
 

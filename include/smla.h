@@ -167,6 +167,10 @@ smla_status smla_load_crossover(const char* json_path);
 /* Human-readable name of a status. Never NULL. */
 const char* smla_status_string(smla_status s);
 
+/* Text of the last CUDA failure seen by a call on this host thread (the CUDA error name and
+ * the step that failed), or "" if none. The pointer stays valid until the next call. */
+const char* smla_last_error(void);
+
 /* Reads and clears the device-side error word that kernels set when a bounded wait
  * gives up (0 = none). Synchronous: waits for the device. */
 smla_status smla_device_error(int32_t* code);

@@ -21,7 +21,7 @@ KV_BF16, KV_FP8 = 0, 1
 EXPORTS = ("smla_supported", "smla_workspace_size", "smla_prefill", "smla_decode", "smla_decode_static",
            "smla_forward",
            "smla_decode_max_tokens", "smla_set_crossover", "smla_load_crossover", "smla_status_string",
-           "smla_device_error", "smla_set_timing_events", "smla_struct_size", "smla_version")
+           "smla_device_error", "smla_last_error", "smla_set_timing_events", "smla_struct_size", "smla_version")
 
 
 class SmlaError(RuntimeError):
@@ -75,6 +75,7 @@ def load(path: Optional[str] = None):
         "smla_load_crossover": ([ctypes.c_char_p], ctypes.c_int),
         "smla_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "smla_device_error": ([ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+        "smla_last_error": ([], ctypes.c_char_p),
         "smla_set_timing_events": ([vp, vp], ctypes.c_int),
         "smla_struct_size": ([ctypes.c_int32], ctypes.c_size_t),
         "smla_version": ([], ctypes.c_int32),
@@ -99,6 +100,8 @@ def _check(st: int, what: str, call=None):
         reason = ""
         if call is not None and st in (SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED):
             reason = " (" + supported(call)[1] + ")"
+        elif st == SMLA_ERR_CUDA:
+            reason = " (" + load().smla_last_error().decode() + ")"
         raise SmlaError(st, f"{what} failed: {status_string(st)}{reason}")
 
 

@@ -156,22 +156,27 @@ Plan make_plan(const smla_params* p, bool split_k) {
   pl.groups = (p->H + kMaxGroupHeads - 1) / kMaxGroupHeads;
   pl.heads_per_group = (p->H + pl.groups - 1) / pl.groups;
   pl.nh = pl.heads_per_group <= 16 ? 16 : (pl.heads_per_group <= 32 ? 32 : 64);
-  pl.total_tiles = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
-  pl.splits = 1;
-  pl.tiles_per_split = pl.total_tiles;
-  if (split_k && p->T > 0) {
-    const long long base = static_cast<long long>(p->T) * pl.groups;
-    const long long sms = sm_count();
-    long long s = sms / std::max<long long>(1, base);
-    s = std::max<long long>(1, std::min<long long>(s, pl.total_tiles));
-    pl.tiles_per_split = static_cast<int>((pl.total_tiles + s - 1) / s);
-    pl.splits = (pl.total_tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
+  pl.tiles_per_item = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
+  pl.n_items = static_cast<long long>(p->T) * pl.groups;
+  pl.total_tiles = pl.n_items * pl.tiles_per_item;
+  const long long sms = sm_count();
+  pl.split = split_k ? 1 : 0;
+  pl.max_slots = 1;
+  if (pl.split) {
+    // Contiguous flat tile ranges, one per persistent CTA; an item spans at most
+    // ceil(tiles_per_item * nctas / total) + 1 ranges.
+    pl.nctas = static_cast<int>(std::max<long long>(1, std::min(sms, pl.total_tiles)));
+    const long long span = (static_cast<long long>(pl.tiles_per_item) * pl.nctas + pl.total_tiles - 1) /
+                           std::max<long long>(1, pl.total_tiles);
+    pl.max_slots = static_cast<int>(std::min<long long>(pl.nctas, span + 1));
+  } else {
+    pl.nctas = static_cast<int>(std::max<long long>(1, std::min(sms, pl.n_items)));
   }
   pl.part_o_bytes = 0;
   pl.workspace_bytes = 0;
-  if (pl.splits > 1) {
-    const size_t n = static_cast<size_t>(pl.splits) * p->T * p->H;
-    pl.part_o_bytes = (n * kDv * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  if (pl.split && p->T > 0) {
+    const size_t n = static_cast<size_t>(pl.max_slots) * p->T * p->H;
+    pl.part_o_bytes = (n * kDv * sizeof(uint16_t) + 255) & ~static_cast<size_t>(255);
     pl.workspace_bytes = pl.part_o_bytes + ((n * sizeof(float) + 255) & ~static_cast<size_t>(255));
   }
   return pl;
@@ -195,6 +200,9 @@ KvSetDev to_dev(const smla_kv_set& s) {
   return d;
 }
 
+// ------------------------------------------------------------------ last CUDA error
+thread_local char g_last_error[256] = {0};
+
 // ------------------------------------------------------------------ timing hook
 std::atomic<void*> g_ev_start{nullptr};
 std::atomic<void*> g_ev_stop{nullptr};
@@ -205,7 +213,7 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
   if (st != SMLA_OK) return st;
   if (p->T == 0) return SMLA_OK;
   const Plan pl = make_plan(p, split_k);
-  if (pl.splits > 1) {
+  if (pl.split) {
     if (p->workspace == nullptr || p->workspace_bytes < pl.workspace_bytes ||
         (reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
       return SMLA_ERR_WORKSPACE;
@@ -221,8 +229,8 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
   a.out_stride_h = p->out_stride_h;
   a.lse = p->lse;
   a.lse_stride_t = p->lse_stride_t;
-  if (pl.splits > 1) {
-    a.part_o = static_cast<float*>(p->workspace);
+  if (pl.split) {
+    a.part_o = p->workspace;
     a.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(p->workspace) + pl.part_o_bytes);
   }
   a.set[0] = to_dev(p->main);
@@ -231,14 +239,17 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
     a.set[1] = to_dev(*p->extra);
     a.nsets = 2;
   }
-  a.total_tiles = pl.total_tiles;
+  a.tiles_per_item = pl.tiles_per_item;
   a.T = p->T;
   a.H = p->H;
   a.num_seqs = p->num_seqs;
   a.groups = pl.groups;
   a.heads_per_group = pl.heads_per_group;
-  a.splits = pl.splits;
-  a.tiles_per_split = pl.tiles_per_split;
+  a.split = pl.split;
+  a.nctas = pl.nctas;
+  a.max_slots = pl.max_slots;
+  a.n_items = pl.n_items;
+  a.total_tiles = pl.total_tiles;
   a.scale_log2 = p->sm_scale * 1.4426950408889634f;
   const cudaError_t e = launch_attention(a, pl, stream, static_cast<cudaEvent_t>(g_ev_start.load()),
                                          static_cast<cudaEvent_t>(g_ev_stop.load()));
@@ -260,6 +271,11 @@ int32_t default_max_tokens(int32_t H) {
 }
 
 }  // namespace
+
+void note_cuda_error(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
 }  // namespace smla
 
 using namespace smla;
@@ -373,10 +389,16 @@ const char* smla_status_string(smla_status s) {
   return "unknown smla_status";
 }
 
+const char* smla_last_error(void) { return g_last_error; }
+
 smla_status smla_device_error(int32_t* code) {
   if (code == nullptr) return SMLA_ERR_INVALID;
   int c = 0;
-  if (read_and_clear_device_error(&c) != cudaSuccess) return SMLA_ERR_CUDA;
+  const cudaError_t e = read_and_clear_device_error(&c);
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "reading the device error word");
+    return SMLA_ERR_CUDA;
+  }
   *code = c;
   return c == 0 ? SMLA_OK : SMLA_ERR_DEVICE;
 }

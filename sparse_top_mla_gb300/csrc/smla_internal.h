@@ -41,17 +41,19 @@ struct AttnArgs {
   int64_t out_stride_t, out_stride_h;
   float* lse;
   int64_t lse_stride_t;
-  float* part_o;    // [splits, T, H, 512] (decode split-K only)
-  float* part_lse;  // [splits, T, H], base-2 log-sum-exp
-  int* err;         // device error word
+  void* part_o;     // bf16 [max_slots, T, H, 512] normalised partial O (split schedule only)
+  float* part_lse;  // [max_slots, T, H] base-2 log-sum-exp of each partial
   KvSetDev set[2];
   int32_t nsets;
-  int32_t total_tiles;
+  int32_t tiles_per_item;  // tiles of one (token, head group) item: main tiles then extra tiles
   int32_t T, H, num_seqs;
   int32_t groups;          // head groups per token
   int32_t heads_per_group;
-  int32_t splits;          // CTAs per (token, group)
-  int32_t tiles_per_split;
+  int32_t split;           // 0: whole items per CTA, final outputs; 1: contiguous tile ranges, partials
+  int32_t nctas;           // persistent CTAs (grid size)
+  int32_t max_slots;       // partial slots per item (split schedule)
+  int64_t n_items;         // T * groups
+  int64_t total_tiles;     // n_items * tiles_per_item
   float scale_log2;        // sm_scale * log2(e)
 };
 
@@ -59,19 +61,34 @@ struct Plan {
   int groups;
   int heads_per_group;
   int nh;  // MMA N: 16, 32 or 64
-  int splits;
-  int tiles_per_split;
-  int total_tiles;
+  int split;
+  int nctas;
+  int max_slots;
+  int tiles_per_item;
+  long long n_items;
+  long long total_tiles;
   size_t part_o_bytes;
   size_t workspace_bytes;
 };
 
-// Launches the attention kernel (final outputs when args.splits == 1, partials otherwise)
-// and, for splits > 1, the combine kernel. Returns cudaSuccess or the launch error.
+// First tile of CTA c in the split schedule: floor(c * total / nctas).
+__host__ __device__ inline long long split_lo(long long c, long long total, long long nctas) {
+  return c * total / nctas;
+}
+// The CTA whose split-schedule tile range contains flat tile x.
+__host__ __device__ inline long long split_owner(long long x, long long total, long long nctas) {
+  return ((x + 1) * nctas - 1) / total;
+}
+
+// Launches the persistent attention kernel (final outputs, or partials for the split
+// schedule) and, for the split schedule, the combine kernel. Returns cudaSuccess or the
+// launch error.
 cudaError_t launch_attention(const AttnArgs& args, const Plan& plan, cudaStream_t stream,
                              cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
-int* device_error_word();  // address of the device error word (host-side query helper)
 cudaError_t read_and_clear_device_error(int* code);
+
+// Records a CUDA failure for smla_last_error (thread-local).
+void note_cuda_error(cudaError_t e, const char* where);
 
 }  // namespace smla

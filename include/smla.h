@@ -76,7 +76,7 @@ typedef struct {
   int64_t row_stride_bytes;   /* >= row bytes (1152 / 656), multiple of 16; padded rows allowed */
   int64_t page_stride_bytes;  /* >= 64 * row_stride_bytes, multiple of 16 */
   int32_t page_size;          /* must be 64 (checked: a wrong page size must not run) */
-  int32_t num_pages;          /* physical pages in `cache` (bounds for block_table entries) */
+  int32_t num_pages;          /* physical pages in `cache` (bounds for block_table entries); <= 2^25 */
   const int32_t* block_table; /* device [num_seqs, bt_stride]: logical page -> physical page */
   int32_t bt_stride;          /* >= 1 */
   const int32_t* seq_lens;    /* device [num_seqs]: valid positions per sequence */

@@ -69,6 +69,10 @@ smla_status check_set(const smla_kv_set& s, const char* name, Why& why) {
     why.set("%s: num_pages=%d and bt_stride=%d must be >= 1", name, s.num_pages, s.bt_stride);
     return SMLA_ERR_INVALID;
   }
+  if (s.num_pages > kMaxPages) {
+    why.set("%s.num_pages=%d unsupported: at most %d pages (2^31 cache rows)", name, s.num_pages, kMaxPages);
+    return SMLA_ERR_UNSUPPORTED;
+  }
   if (s.topk < 1) {
     why.set("%s.topk=%d unsupported: accepted topk >= 1", name, s.topk);
     return SMLA_ERR_UNSUPPORTED;

@@ -14,6 +14,7 @@ constexpr int kTile = 128;      // gathered rows per tile = MMA M
 constexpr int kRowBf16 = 1152;  // bytes of a bf16 row
 constexpr int kRowFp8 = 656;    // bytes of an fp8 row: 512 e4m3 + 4 fp32 scales + 64 bf16 rope
 constexpr int kMaxGroupHeads = 64;
+constexpr int kMaxPages = 1 << 25;  // a cache row is addressed as (page << 6 | row) in 31 bits
 
 struct KvSetDev {
   const uint8_t* cache;

@@ -2,22 +2,28 @@
 //
 // Persistent, warp-specialised kernel. Each CTA (one per SM) walks a stream of tiles; a tile
 // is 128 gathered cache rows of one work item (query token t, head group g). Roles:
-//   warps 0-3   softmax + epilogue (thread i owns gathered row i = TMEM lane i); lane 0 of
-//               warp 3 also issues every tcgen05 MMA and commit, at fixed points of the
-//               softmax program (a separate issue warp would push the block past the
-//               register budget of 640 threads x 96 registers)
-//   warps 4-19  loaders: resolve indices -> cache rows, keep the next tile's raw rows in
-//               registers, and store each 128-channel block pair into shared memory as
-//               soon as the previous tile's PV has released it (FP8 rows are dequantised
-//               to bf16 on the way: e4m3 * per-128-channel scale)
+//   warps 0-3   softmax + epilogue; thread i owns gathered row i of every tile (= TMEM lane i)
+//               and also resolves that row's index -> cache row offset three tiles ahead
+//               (index, then block table and sequence length, then the byte offset), so the
+//               loaders only read finished offsets from shared memory. Warp 3 runs the MMA
+//               issue stream; its lane 0 issues every tcgen05 MMA and commit.
+//   warps 4-11  loaders: keep the next tile's raw rows in registers and store each 128-channel
+//               block pair into shared memory as soon as the previous tile's PV has released it
+//               (FP8 rows are dequantised to bf16 on the way: e4m3 * per-128-channel scale)
 // Per tile the tensor core computes
 //   S^T[128 x NH]  = K_tile[128 x 576] . Q^T          (M = gathered rows, N = heads)
 //   O^T[512 x NH] += V^T[512 x 128] . P^T[128 x NH]  (M = value channels, 4 blocks)
 //   L[128 x NH]   += 1[128 x 128] . P^T[128 x NH]    (row sums of P, every lane equal)
 // with S^T, L and O^T in TMEM. V is the first 512 channels of the same gathered tile (the
-// tile is read K-major for QK^T and MN-major for PV). The issuing thread interleaves PV of
-// tile j with QK^T of tile j+1 block by block, so the loaders refill the blocks PV has
-// finished with while the tensor core keeps working.
+// tile is read K-major for QK^T and MN-major for PV). For tile j the issuing thread queues PV
+// of all four block pairs (one commit each) and the row sums, then QK^T of tile j+1 block by
+// block as the loaders refill the blocks PV has finished with.
+//
+// Softmax: P = 2^(s*scale*log2e - m) against per-head running maxima m. A tile whose scores
+// stay within 2^8 of the maxima (the common case) needs no cross-warp step: the warps write
+// P^T and arrive; the issuing thread checks a shared overflow flag and, only if it is set,
+// sends every softmax warp through the rescale pass (new maxima, O^T and L rescaled, P
+// recomputed) before it issues PV. The first tile of an item always takes the max pass.
 //
 // Schedules: whole items per CTA (prefill; the epilogue writes O and LSE), or contiguous
 // flat tile ranges per CTA (split-K decode; every item segment writes a normalised partial
@@ -45,9 +51,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kSmWarps = 4;
-constexpr int kLdWarps = 16;
+constexpr int kLdWarps = 8;
 constexpr int kLdThreads = kLdWarps * 32;
-constexpr int kThreads = (kSmWarps + kLdWarps) * 32;  // 640
+constexpr int kThreads = (kSmWarps + kLdWarps) * 32;  // 384
+constexpr int kLdRows = kTile / (kLdThreads / 8);      // rows per loader thread: 4
 constexpr int kIssueWarp = kSmWarps - 1;               // its lane 0 issues the MMAs
 constexpr int kKBlocks = 9;                            // 576 channels / 64 per 128-byte row
 constexpr int kBlockBytes = kTile * 128;               // one 64-channel block of the tile: 16 KB
@@ -60,14 +67,17 @@ constexpr int kErrTimeout = 1;
 template <int NH>
 struct Smem {
   static constexpr int kQOff = kTileBytes;
-  static constexpr int kRedOff = kQOff + kKBlocks * NH * 128;  // float [4][64]
+  static constexpr int kRedOff = kQOff + kKBlocks * NH * 128;  // float [4][64] per-warp column maxima
   static constexpr int kMOff = kRedOff + 4 * 64 * 4;            // float [64] running max (base 2)
-  static constexpr int kAlphaOff = kMOff + 64 * 4;              // float [64]
+  static constexpr int kMUseOff = kMOff + 64 * 4;               // float [64] exponent offset (0 while max = -inf)
+  static constexpr int kThrOff = kMUseOff + 64 * 4;             // float [64] s*scale - m_use above this: rescale
+  static constexpr int kAlphaOff = kThrOff + 64 * 4;            // float [64] rescale factor
   static constexpr int kFinOff = kAlphaOff + 64 * 4;            // float [64] output factor per head
-  static constexpr int kRowOff = kFinOff + 64 * 4;              // int64 [4][128] row byte offsets (-1 = masked)
-  static constexpr int kBarOff = kRowOff + 4 * 128 * 8;         // mbarriers
-  static constexpr int kNumBars = 20;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, flags, votes
+  static constexpr int kRowOff = kFinOff + 64 * 4;              // int32 [4][128] rows: page << 6 | row (-1 = masked)
+  static constexpr int kResOff = kRowOff + 4 * kTile * 4;       // int32 [2][5][128] index-resolution staging
+  static constexpr int kBarOff = kResOff + 2 * 5 * kTile * 4;   // mbarriers
+  static constexpr int kNumBars = 24;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, flags
   static constexpr int kOnesOff = kMiscOff + 128;               // 128 B of bf16 1.0 (row-sum operand)
   static constexpr int kBytes = kOnesOff + 128;
   static constexpr int kAlloc = kBytes + 1024;                  // + alignment slack
@@ -75,12 +85,15 @@ struct Smem {
 static_assert(Smem<64>::kAlloc <= 232448, "shared memory budget");
 
 // barrier indices
-constexpr int kBarFull = 0;     // [9] tile block kb stored (16 loader warps arrive)
-constexpr int kBarSFull = 9;    // S^T of the tile is in TMEM (tcgen05.commit)
-constexpr int kBarPReady = 10;  // P^T in smem, O/L rescaled (4 softmax warps arrive)
-constexpr int kBarPvDone = 11;  // [4] PV block pair done (tcgen05.commit)
-constexpr int kBarRow = 15;     // [4] row offsets of tile j in slot j&3 (16 loader warps arrive)
-constexpr int kBarSm = 19;      // barrier among the 128 softmax threads (every thread arrives)
+constexpr int kBarFullA = 0;      // tile blocks 0-3 stored (8 loader warps arrive)
+constexpr int kBarFullB = 1;      // tile blocks 4-8 stored (8 loader warps arrive)
+constexpr int kBarSFull = 9;      // S^T of the tile is in TMEM (tcgen05.commit)
+constexpr int kBarPReady = 10;    // P^T in smem (4 softmax warps arrive)
+constexpr int kBarPvDone = 11;    // [4] PV block pair done (tcgen05.commit)
+constexpr int kBarRow = 15;       // [4] rows of tile j in slot j&3 (softmax warps 0-2 arrive)
+constexpr int kBarSm = 19;        // barrier among the 128 softmax threads (every thread arrives)
+constexpr int kBarDecision = 20;  // the issuing thread has read the overflow flag of the tile
+constexpr int kBarPFixed = 21;    // rescale pass done, P^T rewritten (4 softmax warps arrive)
 
 template <int NH>
 struct TmemCols {
@@ -93,14 +106,17 @@ struct TmemCols {
 struct Shared {
   uint8_t* base;
   uint32_t tile, q;
-  float *red, *m_run, *alpha, *fin;
-  int64_t* rowoff;
+  float *red, *m_run, *m_use, *thr, *alpha, *fin;
+  int32_t* rowoff;
+  uint32_t res;     // staging of the index-resolution loads (cp.async destination)
+  int32_t* resp;    // the same staging, generic pointer
   uint32_t bars;
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   volatile int* rescale_flag;
-  volatile int* vote;  // [2] per-tile "a max must move" flags
-  uint32_t ones;       // 128 B of bf16 1.0
+  volatile int* overflow;  // [2] a score of the tile passed its threshold (by tile parity)
+  volatile int* decision;  // [2] the tile takes the rescale pass (by tile parity)
+  uint32_t ones;           // 128 B of bf16 1.0
   __device__ uint32_t bar(int i) const { return bars + 8u * i; }
 };
 
@@ -138,26 +154,34 @@ __device__ __forceinline__ bool sm_sync(const Shared& sh, uint32_t& phase) {
 }
 
 // ------------------------------------------------------------------ tile stream
-struct TileRef {
-  long long item;
+// Position in the CTA's tile stream: work item and tile within the item. Whole-item schedule:
+// items blockIdx.x, blockIdx.x + nctas, ...; split schedule: consecutive flat tiles from lo.
+struct Cursor {
+  uint32_t item;
   int tile;
-  bool first, last;
+  __device__ __forceinline__ void init(const AttnArgs& a, long long lo) {
+    if (a.split) {
+      item = static_cast<uint32_t>(lo / a.tiles_per_item);
+      tile = static_cast<int>(lo - static_cast<long long>(item) * a.tiles_per_item);
+    } else {
+      item = blockIdx.x;
+      tile = 0;
+    }
+  }
+  __device__ __forceinline__ void next(const AttnArgs& a) {
+    if (++tile == a.tiles_per_item) {
+      tile = 0;
+      item += a.split ? 1u : static_cast<uint32_t>(a.nctas);
+    }
+  }
 };
 
-__device__ __forceinline__ TileRef tile_ref(const AttnArgs& a, long long lo, int n, int j) {
-  TileRef r;
-  if (a.split) {
-    const long long x = lo + j;
-    r.item = x / a.tiles_per_item;
-    r.tile = static_cast<int>(x - r.item * a.tiles_per_item);
-  } else {
-    const int k = j / a.tiles_per_item;
-    r.item = blockIdx.x + static_cast<long long>(k) * a.nctas;
-    r.tile = j - k * a.tiles_per_item;
-  }
-  r.first = r.tile == 0 || j == 0;
-  r.last = r.tile == a.tiles_per_item - 1 || j == n - 1;
-  return r;
+// At most two head groups per token (H <= 128, 64 heads per group).
+__device__ __forceinline__ uint32_t item_token(const AttnArgs& a, uint32_t item) {
+  return a.groups == 2 ? item >> 1 : item;
+}
+__device__ __forceinline__ int item_head0(const AttnArgs& a, uint32_t item) {
+  return a.groups == 2 ? static_cast<int>(item & 1u) * a.heads_per_group : 0;
 }
 
 __device__ __forceinline__ int set_of(const AttnArgs& a, int tile) {
@@ -168,52 +192,77 @@ __device__ __forceinline__ int set_of(const AttnArgs& a, int tile) {
 // array would force a local-memory copy of the parameters).
 #define SET_FIELD(a, sid, f) ((sid) ? (a).set[1].f : (a).set[0].f)
 
-// Index resolution (entry -> cache row byte offset, -1 when masked), split into three phases
-// whose loads only depend on the previous phase, so the loaders can issue each phase right
-// after a tile store and consume it a tile later.
-struct Resolve {
-  int seq, seqlen, idx[2], page[2];
+// ------------------------------------------------------------------ index resolution
+// Entry -> cache row (page << 6 | row in page, -1 when masked) in three phases whose loads only
+// depend on the previous phase; a softmax thread runs each phase one tile after the previous
+// one. The loads are asynchronous copies into a shared staging area (double-buffered by tile
+// parity), so no load result waits in a register for a tile.
+constexpr int kResIdx = 0, kResTl = 1, kResSeq = 2, kResPage = 3, kResLen = 4;
+__device__ __forceinline__ int res_slot(int jt, int field, int r) { return ((jt & 1) * 5 + field) * kTile + r; }
+
+struct ResA {  // phase A issued: entry number, set, which copies were made (1 index, 2 length limit)
+  int e, sid, flags;
+};
+struct ResB {  // phase B issued: index, set, which copies were made (1 page, 2 sequence length)
+  int idx, sid, flags;
 };
 
-__device__ __forceinline__ void resolve_a(const AttnArgs& a, long long item, int tile, int rg, Resolve& R) {
-  const int t = static_cast<int>(item / a.groups);
-  const int sid = set_of(a, tile);
-  const int base = (tile - (sid ? a.set[0].ntiles : 0)) * kTile + rg;
-  int width = SET_FIELD(a, sid, topk);
+__device__ __forceinline__ void res_a(const AttnArgs& a, const Shared& sh, const Cursor& c, int jt, int r, ResA& R) {
+  const uint32_t t = item_token(a, c.item);
+  const int sid = set_of(a, c.tile);
+  R.sid = sid;
+  R.e = (c.tile - (sid ? a.set[0].ntiles : 0)) * kTile + r;
+  R.flags = 0;
+  if (R.e < SET_FIELD(a, sid, topk)) {
+    const int32_t* ip = SET_FIELD(a, sid, indices) + static_cast<int64_t>(t) * SET_FIELD(a, sid, idx_stride);
+    cp_async4(sh.res + 4 * res_slot(jt, kResIdx, r), ip + R.e);
+    R.flags |= 1;
+  }
   const int32_t* tl = SET_FIELD(a, sid, topk_length);
-  if (tl != nullptr) width = min(width, max(0, __ldg(tl + t)));
-  R.seq = __ldg(a.token_seq + t);
-  const int32_t* ip = SET_FIELD(a, sid, indices) + static_cast<int64_t>(t) * SET_FIELD(a, sid, idx_stride);
-#pragma unroll
-  for (int k = 0; k < 2; ++k) R.idx[k] = (base + 64 * k < width) ? __ldg(ip + base + 64 * k) : -1;
+  if (tl != nullptr) {
+    cp_async4(sh.res + 4 * res_slot(jt, kResTl, r), tl + t);
+    R.flags |= 2;
+  }
+  cp_async4(sh.res + 4 * res_slot(jt, kResSeq, r), a.token_seq + t);
 }
 
-__device__ __forceinline__ void resolve_b(const AttnArgs& a, int tile, Resolve& R) {
-  const int sid = set_of(a, tile);
-  const bool seq_ok = R.seq >= 0 && R.seq < a.num_seqs;
-  const int32_t bts = SET_FIELD(a, sid, bt_stride);
-  R.seqlen = seq_ok ? __ldg(SET_FIELD(a, sid, seq_lens) + R.seq) : 0;
-  const int32_t* bt = SET_FIELD(a, sid, block_table) + static_cast<int64_t>(seq_ok ? R.seq : 0) * bts;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int i = R.idx[k];
-    R.page[k] = (seq_ok && i >= 0 && (i >> 6) < bts) ? __ldg(bt + (i >> 6)) : -1;
+// Needs phase A's copies complete.
+__device__ __forceinline__ void res_b(const AttnArgs& a, const Shared& sh, const ResA& A, int jt, int r, ResB& B) {
+  const int sid = A.sid;
+  const int tl = (A.flags & 2) ? sh.resp[res_slot(jt, kResTl, r)] : 0x7fffffff;
+  const int seq = sh.resp[res_slot(jt, kResSeq, r)];
+  B.sid = sid;
+  B.idx = ((A.flags & 1) && A.e < tl) ? sh.resp[res_slot(jt, kResIdx, r)] : -1;
+  B.flags = 0;
+  if (seq >= 0 && seq < a.num_seqs) {
+    cp_async4(sh.res + 4 * res_slot(jt, kResLen, r), SET_FIELD(a, sid, seq_lens) + seq);
+    B.flags |= 2;
+    const int32_t bts = SET_FIELD(a, sid, bt_stride);
+    if (B.idx >= 0 && (B.idx >> 6) < bts) {
+      cp_async4(sh.res + 4 * res_slot(jt, kResPage, r),
+                SET_FIELD(a, sid, block_table) + static_cast<int64_t>(seq) * bts + (B.idx >> 6));
+      B.flags |= 1;
+    }
   }
 }
 
-__device__ __forceinline__ void resolve_c(const AttnArgs& a, int tile, const Resolve& R, int64_t* off) {
-  const int sid = set_of(a, tile);
-  const int32_t np = SET_FIELD(a, sid, num_pages);
-  const int64_t ps = SET_FIELD(a, sid, page_stride);
-  const int64_t rs = SET_FIELD(a, sid, row_stride);
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int i = R.idx[k];
-    const int p = R.page[k];
-    off[k] = (i >= 0 && i < R.seqlen && p >= 0 && p < np)
-                 ? static_cast<int64_t>(p) * ps + static_cast<int64_t>(i & 63) * rs
-                 : -1;
-  }
+// Needs phase B's copies complete.
+__device__ __forceinline__ int32_t res_c(const AttnArgs& a, const Shared& sh, const ResB& B, int jt, int r) {
+  const int seqlen = (B.flags & 2) ? sh.resp[res_slot(jt, kResLen, r)] : 0;
+  const int page = (B.flags & 1) ? sh.resp[res_slot(jt, kResPage, r)] : -1;
+  return (B.idx >= 0 && B.idx < seqlen && page >= 0 && page < SET_FIELD(a, B.sid, num_pages))
+             ? (page << 6) | (B.idx & 63)
+             : -1;
+}
+
+// Row r of tile jt -> shared slot jt&3, read by the loaders and by the softmax thread of row r.
+__device__ __forceinline__ void publish_row(const Shared& sh, int jt, int r, int32_t row) {
+  sh.rowoff[(jt & 3) * kTile + r] = row;
+}
+// The warp's rows of tile jt are published: one arrival per warp.
+__device__ __forceinline__ void publish_done(const Shared& sh, int jt, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sh.bar(kBarRow + (jt & 3)));
 }
 
 // ------------------------------------------------------------------ helpers
@@ -274,32 +323,42 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizz
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// TMEM columns [c, c+W) of this warp's lanes into v (W = 16 or 32), waited.
+template <int W>
+__device__ __forceinline__ void tmem_load(uint32_t addr, float* v) {
+  if constexpr (W == 32) {
+    tmem_ld32_nw(addr, v);
+    tmem_ld_wait32(v);
+  } else {
+    tmem_ld16_nw(addr, v);
+    tmem_ld_wait16(v);
+  }
+}
+
 // ------------------------------------------------------------------ loader role
-// Thread u (0..511) owns rows rg and rg+64 (rg = u/8) and the 16-byte chunk lane8 = u%8
+// Thread u (0..255) owns rows rg + 32k, k < 4 (rg = u/8) and the 16-byte chunk lane8 = u%8
 // of every 128-byte row segment, so 8 consecutive threads read 128 contiguous bytes.
 //
 // Register staging (4 slots of one 16-byte chunk per row): an FP8 block pair needs one slot,
 // so FP8 tiles are loaded a whole tile ahead (block pair bp of tile j+1 is issued as soon as
 // block pair bp of tile j is stored); a bf16 block pair needs two slots, so bf16 tiles are
-// loaded half a tile ahead (block pair bp+2 after bp is stored). Index resolution runs in
-// three phases one tile apart (A: index and sequence loads, B: block-table and length loads,
-// C: offsets), finishing two tiles ahead of use.
+// loaded half a tile ahead (block pair bp+2 after bp is stored).
 struct LdData {
-  uint4 d[4][2];   // [slot][row k]
-  float sc[4][2];  // fp8 scale of the block pair held in slot [s][row k]
-  uint4 rope[2];
+  uint4 d[4][kLdRows];   // [slot][row k]
+  float sc[4][kLdRows];  // fp8 scale of the block pair held in slot [s][row k]
+  uint4 rope[kLdRows];
 };
 
 template <int S>  // fp8 block pair -> slot S
 __device__ __forceinline__ void ld_issue_fp8(const uint8_t* cache, const int64_t* off, int lane8, int bp, LdData& D) {
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kLdRows; ++k) {
     D.d[S][k] = make_uint4(0, 0, 0, 0);
     D.sc[S][k] = 0.f;
     if (off[k] >= 0) {
       const uint8_t* row = cache + off[k];
       D.d[S][k] = ldg_nc_v4(row + 128 * bp + 16 * lane8);
-      D.sc[S][k] = __ldg(reinterpret_cast<const float*>(row + 512) + bp);
+      D.sc[S][k] = ldg_nc_f32(row + 512 + 4 * bp);
     }
   }
 }
@@ -307,7 +366,7 @@ __device__ __forceinline__ void ld_issue_fp8(const uint8_t* cache, const int64_t
 template <int P>  // bf16 block pair -> slots 2P, 2P+1
 __device__ __forceinline__ void ld_issue_bf16(const uint8_t* cache, const int64_t* off, int lane8, int bp, LdData& D) {
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kLdRows; ++k) {
     D.d[2 * P][k] = make_uint4(0, 0, 0, 0);
     D.d[2 * P + 1][k] = make_uint4(0, 0, 0, 0);
     if (off[k] >= 0) {
@@ -321,31 +380,35 @@ __device__ __forceinline__ void ld_issue_bf16(const uint8_t* cache, const int64_
 __device__ __forceinline__ void ld_issue_rope(int fmt, const uint8_t* cache, const int64_t* off, int lane8,
                                               LdData& D) {
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < kLdRows; ++k) {
     D.rope[k] = make_uint4(0, 0, 0, 0);
     if (off[k] >= 0) D.rope[k] = ldg_nc_v4(cache + off[k] + (fmt == 0 ? 1024 : 528) + 16 * lane8);
   }
 }
 
+// An fp8 chunk of 16 channels becomes two bf16 chunks of block 2bp + lane8/4. The threads
+// of the second block store their two chunks in the opposite order, so the 8 threads of a
+// store phase always hit 8 different 16-byte bank groups.
 template <int S>
 __device__ __forceinline__ void ld_store_fp8(const Shared& sh, int rg, int lane8, int bp, const LdData& D) {
+  const bool second = (lane8 >> 2) != 0;
+  const uint32_t blk = sh.tile + (2 * bp + (lane8 >> 2)) * kBlockBytes;
+  const int c0 = (lane8 & 3) * 2;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int r = rg + 64 * k;
+  for (int k = 0; k < kLdRows; ++k) {
+    const int r = rg + 32 * k;
     uint4 lo, hi;
     dequant16(D.d[S][k], D.sc[S][k], lo, hi);
-    const int kb = 2 * bp + (lane8 >> 2);
-    const int c0 = (lane8 & 3) * 2;
-    sts_v4(sh.tile + kb * kBlockBytes + swz(r, c0), lo);
-    sts_v4(sh.tile + kb * kBlockBytes + swz(r, c0 + 1), hi);
+    sts_v4(blk + swz(r, c0 + (second ? 1 : 0)), second ? hi : lo);
+    sts_v4(blk + swz(r, c0 + (second ? 0 : 1)), second ? lo : hi);
   }
 }
 
 template <int P>
 __device__ __forceinline__ void ld_store_bf16(const Shared& sh, int rg, int lane8, int bp, const LdData& D) {
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int r = rg + 64 * k;
+  for (int k = 0; k < kLdRows; ++k) {
+    const int r = rg + 32 * k;
     sts_v4(sh.tile + (2 * bp) * kBlockBytes + swz(r, lane8), D.d[2 * P][k]);
     sts_v4(sh.tile + (2 * bp + 1) * kBlockBytes + swz(r, lane8), D.d[2 * P + 1][k]);
   }
@@ -362,7 +425,9 @@ __device__ __forceinline__ void ld_issue_fp8_rt(const uint8_t* cache, const int6
   }
 }
 
-template <int NH>
+// F0, F1: cache formats of the main and the extra set (compile-time, so each kernel carries only
+// the load paths it uses).
+template <int NH, int F0, int F1>
 __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh, long long lo, int n) {
   const int u = threadIdx.x - kSmWarps * 32;
   const int lane = threadIdx.x & 31;
@@ -370,9 +435,9 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   const int rg = u >> 3;
   if (n <= 0) return;
 
-  auto load_q = [&](long long item) {
-    const int t = static_cast<int>(item / a.groups);
-    const int h0 = static_cast<int>(item - static_cast<long long>(t) * a.groups) * a.heads_per_group;
+  auto load_q = [&](uint32_t item) {
+    const uint32_t t = item_token(a, item);
+    const int h0 = item_head0(a, item);
     const int hg = min(a.heads_per_group, a.H - h0);
     const uint16_t* qb = a.q + static_cast<int64_t>(t) * a.q_stride_t;
     for (int e = u; e < NH * 72; e += kLdThreads) {
@@ -385,9 +450,9 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
     }
     cp_async_commit();
   };
-  auto prefetch_q = [&](long long item) {
-    const int t = static_cast<int>(item / a.groups);
-    const int h0 = static_cast<int>(item - static_cast<long long>(t) * a.groups) * a.heads_per_group;
+  auto prefetch_q = [&](uint32_t item) {
+    const uint32_t t = item_token(a, item);
+    const int h0 = item_head0(a, item);
     const int hg = min(a.heads_per_group, a.H - h0);
     for (int e = u; e < hg * 9; e += kLdThreads) {
       const uint16_t* p = a.q + static_cast<int64_t>(t) * a.q_stride_t +
@@ -395,66 +460,61 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
     }
   };
-  auto publish = [&](int jt, const int64_t* off) {  // row validity for the softmax warps
-    if (lane8 == 0) {
-      sh.rowoff[(jt & 3) * 128 + rg] = off[0];
-      sh.rowoff[(jt & 3) * 128 + rg + 64] = off[1];
+  // byte offsets of this thread's rows of tile jt (published by the softmax threads three
+  // tiles ahead of their use); one barrier wait per tile
+  auto get_off = [&](int jt, const Cursor& c, int64_t* off) -> bool {
+    if (!wait_bar_w(sh, sh.bar(kBarRow + (jt & 3)), (jt >> 2) & 1)) return false;
+    const int sid = set_of(a, c.tile);
+    const int64_t ps = SET_FIELD(a, sid, page_stride);
+    const int64_t rs = SET_FIELD(a, sid, row_stride);
+#pragma unroll
+    for (int k = 0; k < kLdRows; ++k) {
+      const int32_t p = sh.rowoff[(jt & 3) * kTile + rg + 32 * k];
+      off[k] = p < 0 ? -1 : static_cast<int64_t>(p >> 6) * ps + static_cast<int64_t>(p & 63) * rs;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sh.bar(kBarRow + (jt & 3)));
+    return true;
   };
-  auto fmt_of = [&](int jt) { return SET_FIELD(a, set_of(a, tile_ref(a, lo, n, jt).tile), format); };
-  auto cache_of = [&](int jt) { return SET_FIELD(a, set_of(a, tile_ref(a, lo, n, jt).tile), cache); };
 
-  // resolution pipeline: tile 0 now (its loads go out at once), then tile 1, then tile 2
-  // through phase A
-  int64_t off_cur[2], off_nxt[2] = {-1, -1};
-  Resolve RA, RB;
+  auto fmt_of = [&](const Cursor& c) { return F0 == F1 ? F0 : (set_of(a, c.tile) ? F1 : F0); };
+  auto cache_of = [&](const Cursor& c) { return SET_FIELD(a, set_of(a, c.tile), cache); };
+
+  Cursor cur;
+  cur.init(a, lo);
   LdData D;
-  int fmt_cur = fmt_of(0);
-  const uint8_t* cache_cur = cache_of(0);
-  int fmt_nxt = n > 1 ? fmt_of(1) : 0;
-  const uint8_t* cache_nxt = n > 1 ? cache_of(1) : nullptr;
+  int64_t off_cur[kLdRows], off_nxt[kLdRows];
+  prefetch_q(cur.item);
+  if (!get_off(0, cur, off_cur)) return;
   {
-    TileRef r = tile_ref(a, lo, n, 0);
-    resolve_a(a, r.item, r.tile, rg, RB);
-    if (r.first) prefetch_q(r.item);
-    resolve_b(a, r.tile, RB);
-    resolve_c(a, r.tile, RB, off_cur);
-    publish(0, off_cur);
-    if (fmt_cur == 1) {
-      ld_issue_fp8<0>(cache_cur, off_cur, lane8, 0, D);
-      ld_issue_fp8<1>(cache_cur, off_cur, lane8, 1, D);
-      ld_issue_fp8<2>(cache_cur, off_cur, lane8, 2, D);
-      ld_issue_fp8<3>(cache_cur, off_cur, lane8, 3, D);
-      ld_issue_rope(1, cache_cur, off_cur, lane8, D);
+    const uint8_t* cache = cache_of(cur);
+    if (fmt_of(cur) == 1) {
+      ld_issue_fp8<0>(cache, off_cur, lane8, 0, D);
+      ld_issue_fp8<1>(cache, off_cur, lane8, 1, D);
+      ld_issue_fp8<2>(cache, off_cur, lane8, 2, D);
+      ld_issue_fp8<3>(cache, off_cur, lane8, 3, D);
+      ld_issue_rope(1, cache, off_cur, lane8, D);
     } else {
-      ld_issue_bf16<0>(cache_cur, off_cur, lane8, 0, D);
-      ld_issue_bf16<1>(cache_cur, off_cur, lane8, 1, D);
-    }
-    if (n > 1) {
-      r = tile_ref(a, lo, n, 1);
-      resolve_a(a, r.item, r.tile, rg, RB);
-      resolve_b(a, r.tile, RB);
-      resolve_c(a, r.tile, RB, off_nxt);
-      publish(1, off_nxt);
-    }
-    if (n > 2) {
-      r = tile_ref(a, lo, n, 2);
-      resolve_a(a, r.item, r.tile, rg, RA);
+      ld_issue_bf16<0>(cache, off_cur, lane8, 0, D);
+      ld_issue_bf16<1>(cache, off_cur, lane8, 1, D);
     }
   }
 
   for (int j = 0; j < n; ++j) {
-    const TileRef tr = tile_ref(a, lo, n, j);
+    const bool first = cur.tile == 0 || j == 0;
     const bool has1 = j + 1 < n;
-    const bool has2 = j + 2 < n;
-    if (has1 && tile_ref(a, lo, n, j + 1).first) prefetch_q(tile_ref(a, lo, n, j + 1).item);
-    int64_t off2[2] = {-1, -1};
+    Cursor nxt = cur;
+    nxt.next(a);
+    if (has1) {
+      if (nxt.tile == 0) prefetch_q(nxt.item);
+      if (!get_off(j + 1, nxt, off_nxt)) return;
+    }
+    const int fmt_cur = fmt_of(cur);
+    const int fmt_nxt = has1 ? fmt_of(nxt) : 0;
+    const uint8_t* cache_cur = cache_of(cur);
+    const uint8_t* cache_nxt = has1 ? cache_of(nxt) : cache_cur;
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
-      if (bp == 0 && tr.first) load_q(tr.item);
+      if (bp == 0 && first) load_q(cur.item);
       if (fmt_cur == 1) {
         ld_store_fp8<bp>(sh, rg, lane8, bp, D);
       } else {
@@ -462,15 +522,13 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       }
       if (bp == 3) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) sts_v4(sh.tile + 8 * kBlockBytes + swz(rg + 64 * k, lane8), D.rope[k]);
+        for (int k = 0; k < kLdRows; ++k) sts_v4(sh.tile + 8 * kBlockBytes + swz(rg + 32 * k, lane8), D.rope[k]);
       }
-      if (bp == 0 && tr.first) cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(sh.bar(kBarFull + 2 * bp));
-        mbar_arrive(sh.bar(kBarFull + 2 * bp + 1));
-        if (bp == 3) mbar_arrive(sh.bar(kBarFull + 8));
+      if (bp == 0 && first) cp_async_wait_all();
+      if (bp & 1) {  // blocks 0-3 (after bp 1) or 4-8 (after bp 3) complete
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sh.bar(bp == 1 ? kBarFullA : kBarFullB));
       }
       // ---- refill the slots this store freed
       if (fmt_cur == 1) {
@@ -484,56 +542,34 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
             ld_issue_bf16<1>(cache_nxt, off_nxt, lane8, 1, D);
           }
         }
-      } else {
-        if (bp == 0) {
-          ld_issue_bf16<0>(cache_cur, off_cur, lane8, 2, D);
-        } else if (bp == 1) {
-          ld_issue_bf16<1>(cache_cur, off_cur, lane8, 3, D);
-          ld_issue_rope(0, cache_cur, off_cur, lane8, D);
-        } else if (has1) {
-          if (fmt_nxt == 0) {
-            ld_issue_bf16<(bp & 1)>(cache_nxt, off_nxt, lane8, bp - 2, D);
-          } else {
-            ld_issue_fp8_rt(cache_nxt, off_nxt, lane8, 2 * (bp - 2), D);
-            ld_issue_fp8_rt(cache_nxt, off_nxt, lane8, 2 * (bp - 2) + 1, D);
-            if (bp == 3) ld_issue_rope(1, cache_nxt, off_nxt, lane8, D);
-          }
+      } else if (bp == 0) {
+        ld_issue_bf16<0>(cache_cur, off_cur, lane8, 2, D);
+      } else if (bp == 1) {
+        ld_issue_bf16<1>(cache_cur, off_cur, lane8, 3, D);
+        ld_issue_rope(0, cache_cur, off_cur, lane8, D);
+      } else if (has1) {
+        if (fmt_nxt == 0) {
+          ld_issue_bf16<(bp & 1)>(cache_nxt, off_nxt, lane8, bp - 2, D);
+        } else {
+          ld_issue_fp8_rt(cache_nxt, off_nxt, lane8, 2 * (bp - 2), D);
+          ld_issue_fp8_rt(cache_nxt, off_nxt, lane8, 2 * (bp - 2) + 1, D);
+          if (bp == 3) ld_issue_rope(1, cache_nxt, off_nxt, lane8, D);
         }
-      }
-      // ---- index resolution pipeline
-      if (bp == 0 && has2) {
-        RB = RA;  // phase A of tile j+2 was issued a tile ago
-        resolve_b(a, tile_ref(a, lo, n, j + 2).tile, RB);
-        if (j + 3 < n) {
-          const TileRef r3 = tile_ref(a, lo, n, j + 3);
-          resolve_a(a, r3.item, r3.tile, rg, RA);
-        }
-      }
-      if (bp == 3 && has2) {
-        resolve_c(a, tile_ref(a, lo, n, j + 2).tile, RB, off2);
-        publish(j + 2, off2);
       }
       return true;
     };
     if (!step(std::integral_constant<int, 0>{}) || !step(std::integral_constant<int, 1>{}) ||
         !step(std::integral_constant<int, 2>{}) || !step(std::integral_constant<int, 3>{}))
       return;
-    off_cur[0] = off_nxt[0];
-    off_cur[1] = off_nxt[1];
-    fmt_cur = fmt_nxt;
-    cache_cur = cache_nxt;
-    if (has2) {
-      off_nxt[0] = off2[0];
-      off_nxt[1] = off2[1];
-      fmt_nxt = fmt_of(j + 2);
-      cache_nxt = cache_of(j + 2);
-    }
+    cur = nxt;
+#pragma unroll
+    for (int k = 0; k < kLdRows; ++k) off_cur[k] = off_nxt[k];
   }
 }
 
 // ------------------------------------------------------------------ MMA issue (one thread)
-// Descriptors are built once; each MMA adds a compile-time byte offset (>> 4) to the start
-// address field, so issuing costs a few instructions per MMA.
+// Descriptors are built once per call; each MMA adds a compile-time byte offset (>> 4) to the
+// start address field, so issuing costs a few instructions per MMA.
 struct MmaDesc {
   uint64_t qk_a, qk_b, pv_a, pv_b, ones;
 };
@@ -549,236 +585,300 @@ __device__ __forceinline__ MmaDesc make_descs(const Shared& sh) {
   return d;
 }
 
-template <int NH, int KB0, int KB1>
-__device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint32_t tmem, int j) {
+// The whole issuing warp runs the issue code (waits are warp-wide); only its lane 0 issues the
+// MMAs and commits, as predicated instructions. A warp whose lanes stay diverged for the length
+// of an issue sequence pays several hundred cycles to reconverge afterwards.
+//
+// QK^T of tile j, waiting once for blocks 0-3 and once for blocks 4-8 (every mbarrier wait in
+// the issue stream lets the tensor pipe run dry for a few hundred cycles). Fully unrolled: in
+// a loop the advancing descriptors cost ~40 cycles per MMA.
+template <int NH>
+__device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint32_t tmem, int j, bool leader) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 0);
 #pragma unroll
-  for (int kb = KB0; kb < KB1; ++kb) {
-    if (!wait_bar(sh, sh.bar(kBarFull + kb), j & 1)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      mma_bf16_ss(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint64_t>((kb * kBlockBytes + ks * 32) >> 4),
-                  d.qk_b + static_cast<uint64_t>((kb * NH * 128 + ks * 32) >> 4), idesc, (kb | ks) != 0);
+  for (int kb = 0; kb < kKBlocks; ++kb) {
+    if (kb == 0 || kb == 4) {
+      if (!wait_bar_w(sh, sh.bar(kb == 0 ? kBarFullA : kBarFullB), j & 1)) return false;
+      tc_fence_after();
     }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16_ss(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint64_t>((kb * kBlockBytes + ks * 32) >> 4),
+                  d.qk_b + static_cast<uint64_t>((kb * NH * 128 + ks * 32) >> 4), idesc, (kb | ks) != 0, leader);
   }
   return true;
 }
 
-template <int NH, int BP>
-__device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint32_t tmem, bool first) {
+// O^T block pair bp (value channels 128bp..128bp+127) += V^T . P^T, then a commit that releases
+// the tile's blocks 2bp, 2bp+1 to the loaders.
+template <int NH>
+__device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint32_t tmem, int bp, bool first,
+                                       bool leader) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 1, 1);
+  const uint64_t da = d.pv_a + static_cast<uint64_t>((2 * bp * kBlockBytes) >> 4);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    mma_bf16_ss(tmem + TmemCols<NH>::kO + BP * NH,
-                d.pv_a + static_cast<uint64_t>((2 * BP * kBlockBytes + ks * 2048) >> 4),
-                d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc, (first && ks == 0) ? 0u : 1u);
-  }
-  mma_commit(sh.bar(kBarPvDone + BP));
+  for (int ks = 0; ks < 8; ++ks)
+    mma_bf16_ss(tmem + TmemCols<NH>::kO + bp * NH, da + static_cast<uint64_t>((ks * 2048) >> 4),
+                d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc, (first && ks == 0) ? 0u : 1u, leader);
+  mma_commit(sh.bar(kBarPvDone + bp), leader);
 }
 
 // Row sums of P for every head: L[m, h] += sum_k 1 * P^T[k, h] (all 128 lanes get the same
 // sums). Same B operand and accumulate rule as PV, so the normalisation uses exactly the bf16
 // P that multiplied V.
 template <int NH>
-__device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first) {
+__device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first, bool leader) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
     mma_bf16_ss(tmem + TmemCols<NH>::kL, d.ones, d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc,
-                (first && ks == 0) ? 0u : 1u);
+                (first && ks == 0) ? 0u : 1u, leader);
 }
 
 // QK^T of the first tile of the stream.
 template <int NH>
-__device__ __forceinline__ bool mma_issue_first(const Shared& sh, const MmaDesc& d, uint32_t tmem) {
-  if (!mma_qk<NH, 0, kKBlocks>(sh, d, tmem, 0)) return false;
-  mma_commit(sh.bar(kBarSFull));
+__device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem, bool leader) {
+  const MmaDesc d = make_descs<NH>(sh);
+  if (!mma_qk<NH>(sh, d, tmem, 0, leader)) return false;
+  mma_commit(sh.bar(kBarSFull), leader);
   return true;
 }
 
-// After the softmax of tile j: PV of tile j block pair by block pair, interleaved with QK^T of
-// tile j+1 as its blocks arrive (the loaders refill a block pair once its PV has finished).
+// After the softmax of tile j: PV of all four block pairs (each with its own commit, so the
+// loaders refill a block pair as soon as it is released) and the row sums (before the last
+// block pair, so its commit covers them), then QK^T of tile j+1 as its blocks arrive.
 template <int NH>
-__device__ __forceinline__ bool mma_issue_after(const AttnArgs& a, const Shared& sh, const MmaDesc& d, uint32_t tmem,
-                                                long long lo, int n, int j) {
-  if (!wait_bar(sh, sh.bar(kBarPReady), j & 1)) return false;
+__device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem, int j, int n, bool first,
+                                                bool leader) {
+  const MmaDesc d = make_descs<NH>(sh);
   tc_fence_after();
-  const bool first = tile_ref(a, lo, n, j).first;
-  mma_pv<NH, 0>(sh, d, tmem, first);
-  mma_pv<NH, 1>(sh, d, tmem, first);
-  if (j + 1 >= n) {
-    mma_pv<NH, 2>(sh, d, tmem, first);
-    mma_rowsum<NH>(d, tmem, first);
-    mma_pv<NH, 3>(sh, d, tmem, first);
-    return true;
+#pragma unroll 1
+  for (int bp = 0; bp < 4; ++bp) {
+    if (bp == 3) mma_rowsum<NH>(d, tmem, first, leader);
+    mma_pv<NH>(sh, d, tmem, bp, first, leader);
   }
-  if (!mma_qk<NH, 0, 2>(sh, d, tmem, j + 1)) return false;
-  mma_pv<NH, 2>(sh, d, tmem, first);
-  if (!mma_qk<NH, 2, 4>(sh, d, tmem, j + 1)) return false;
-  mma_rowsum<NH>(d, tmem, first);
-  mma_pv<NH, 3>(sh, d, tmem, first);
-  if (!mma_qk<NH, 4, kKBlocks>(sh, d, tmem, j + 1)) return false;
-  mma_commit(sh.bar(kBarSFull));
+  if (j + 1 >= n) return true;
+  if (!mma_qk<NH>(sh, d, tmem, j + 1, leader)) return false;
+  mma_commit(sh.bar(kBarSFull), leader);
   return true;
 }
 
 // ------------------------------------------------------------------ softmax / epilogue role
-// P^T (bf16) for 16 heads from S^T chunk c0, using the running maxima; returns whether any score
-// exceeds its head's maximum by more than 2^8 (then the maxima have to move).
+// P^T (bf16) of this thread's row from S^T: p = 2^(s*scale - m_use) per head. Returns whether
+// the row is valid and some head's score passed its threshold (the running max must move).
+// Invalid rows write zeros.
 template <int NH>
-__device__ __forceinline__ bool softmax_chunk(const AttnArgs& a, const Shared& sh, uint32_t s_addr, uint32_t pt, int c0,
-                                              bool valid, int tid) {
-  float s[16];
-  tmem_ld16(s_addr, s);
+__device__ __forceinline__ bool p_pass(const AttnArgs& a, const Shared& sh, uint32_t s_addr, uint32_t pt, bool valid,
+                                       int tid) {
+  constexpr int CW = NH < 32 ? NH : 32;
   bool over = false;
-  uint32_t w[8];
-  const float4* m4 = reinterpret_cast<const float4*>(sh.m_run + c0);
+#pragma unroll 1
+  for (int c0 = 0; c0 < NH; c0 += CW) {
+    float s[CW];
+    tmem_load<CW>(s_addr + c0, s);
+    uint32_t w[CW / 2];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 m = m4[q];
-    const float mv[4] = {m.x, m.y, m.z, m.w};
-    float p[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x = valid ? s[4 * q + e] * a.scale_log2 : -INFINITY;
-      over |= x > mv[e] + kLazyRescaleLog2;
-      p[e] = ex2(x - (mv[e] == -INFINITY ? 0.f : mv[e]));
+    for (int q = 0; q < CW / 4; ++q) {
+      const float4 mu = reinterpret_cast<const float4*>(sh.m_use)[(c0 >> 2) + q];
+      const float4 th = reinterpret_cast<const float4*>(sh.thr)[(c0 >> 2) + q];
+      const float d0 = fmaf(s[4 * q + 0], a.scale_log2, -mu.x);
+      const float d1 = fmaf(s[4 * q + 1], a.scale_log2, -mu.y);
+      const float d2 = fmaf(s[4 * q + 2], a.scale_log2, -mu.z);
+      const float d3 = fmaf(s[4 * q + 3], a.scale_log2, -mu.w);
+      over |= (d0 > th.x) | (d1 > th.y) | (d2 > th.z) | (d3 > th.w);
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(ex2(d0), ex2(d1));
+      const __nv_bfloat162 b1 = __floats2bfloat162_rn(ex2(d2), ex2(d3));
+      w[2 * q] = valid ? *reinterpret_cast<const uint32_t*>(&b0) : 0u;
+      w[2 * q + 1] = valid ? *reinterpret_cast<const uint32_t*>(&b1) : 0u;
     }
-    const __nv_bfloat162 b0 = __floats2bfloat162_rn(p[0], p[1]);
-    const __nv_bfloat162 b1 = __floats2bfloat162_rn(p[2], p[3]);
-    w[2 * q] = *reinterpret_cast<const uint32_t*>(&b0);
-    w[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+    // P^T in the no-swizzle MN-major layout: [head/8][row/8][row%8][head%8]
+#pragma unroll
+    for (int g = 0; g < CW / 8; ++g)
+      sts_v4(pt + ((c0 >> 3) + g) * 2048 + (tid >> 3) * 128 + (tid & 7) * 16,
+             make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]));
   }
-  // P^T in the no-swizzle MN-major layout: [head/8][row/8][row%8][head%8]
-  const uint32_t dst = pt + (c0 >> 3) * 2048 + (tid >> 3) * 128 + (tid & 7) * 16;
-  sts_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-  sts_v4(dst + 2048, make_uint4(w[4], w[5], w[6], w[7]));
-  return over;
+  return over && valid;
+}
+
+// Max pass: per-head maximum of the tile over valid rows, new running maxima (always on the
+// first tile of an item; otherwise only where a maximum passed its threshold), O^T and L
+// rescaled where a maximum moved, then P^T recomputed.
+template <int NH>
+__device__ __forceinline__ bool max_pass(const AttnArgs& a, const Shared& sh, uint32_t tmem_lane, uint32_t pt,
+                                         bool valid, bool first, uint32_t& smph, int tid) {
+  constexpr int CW = NH < 32 ? NH : 32;
+  using TC = TmemCols<NH>;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+#pragma unroll 1
+  for (int c0 = 0; c0 < NH; c0 += CW) {
+    float s[CW];
+    tmem_load<CW>(tmem_lane + TC::kS + c0, s);
+#pragma unroll
+    for (int h = 0; h < CW; ++h) s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
+    warp_col_reduce_store<CW, true>(s, lane, sh.red + warp * 64 + c0);
+  }
+  if (!sm_sync(sh, smph)) return false;
+  if (warp == 0) {
+    bool raised = false;
+    for (int h = lane; h < NH; h += 32) {
+      const float tmax = fmaxf(fmaxf(sh.red[h], sh.red[64 + h]), fmaxf(sh.red[128 + h], sh.red[192 + h]));
+      const float mo = first ? -INFINITY : sh.m_run[h];
+      float m = mo, al = 1.f;
+      if (first || tmax > mo + kLazyRescaleLog2) {
+        m = tmax;
+        al = (mo == -INFINITY) ? 0.f : ex2(mo - tmax);
+        raised = true;
+      }
+      sh.m_run[h] = m;
+      sh.m_use[h] = m == -INFINITY ? 0.f : m;
+      sh.thr[h] = m == -INFINITY ? -INFINITY : kLazyRescaleLog2;
+      sh.alpha[h] = al;
+    }
+    raised = __any_sync(0xffffffffu, raised);
+    if (lane == 0) *sh.rescale_flag = raised ? 1 : 0;
+  }
+  if (!sm_sync(sh, smph)) return false;
+  p_pass<NH>(a, sh, tmem_lane + TC::kS, pt, valid, tid);
+  // O^T and the row sums *= alpha where a running max moved (the previous PV is complete:
+  // S^T of this tile was committed after it)
+  if (!first && *sh.rescale_flag != 0) {
+#pragma unroll 1
+    for (int b = 0; b <= 4; ++b) {
+      const uint32_t col = b < 4 ? TC::kO + b * NH : TC::kL;
+#pragma unroll 1
+      for (int c0 = 0; c0 < NH; c0 += 16) {
+        float o[16];
+        const uint32_t addr = tmem_lane + col + c0;
+        tmem_load<16>(addr, o);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] *= sh.alpha[c0 + i];
+        tmem_st16(addr, o);
+      }
+    }
+    tmem_st_wait();
+  }
+  return true;
 }
 
 template <int NH>
 __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh, uint32_t tmem, long long lo, int n) {
-  constexpr int CW = NH < 32 ? NH : 32;  // columns per reduction pass
+  constexpr int CW = NH < 32 ? NH : 32;
   using TC = TmemCols<NH>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
   const uint32_t pt = sh.tile + 8 * kBlockBytes;
-
-  const bool issuer = warp == kIssueWarp && lane == 0;
-  const MmaDesc md = make_descs<NH>(sh);
   uint32_t smph = 0;
-  if (warp == kIssueWarp) {
-    bool ok = true;
-    if (issuer && n > 0) ok = mma_issue_first<NH>(sh, md, tmem);
-    __syncwarp();
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  int nfix = 0;
+  if (n <= 0) return;
+
+  // ---- index resolution, by warps 0-2 (warp 0 also takes rows 96-127, so the issuing warp
+  // stays free)
+  const int nres = warp == 0 ? 2 : (warp < kIssueWarp ? 1 : 0);
+  const int rrow[2] = {tid, 3 * 32 + lane};
+  auto each = [&](auto&& f) {
+#pragma unroll 1
+    for (int q = 0; q < nres; ++q) f(q);
+  };
+  Cursor rc;
+  rc.init(a, lo);
+  ResA ra[2] = {{0, 0, 0}, {0, 0, 0}};
+  ResB rb[2] = {{-1, 0, 0}, {-1, 0, 0}};
+  // step j: publish tile j+3 (phase C), phase B of tile j+4, phase A of tile j+5; the copies it
+  // waits for were issued by the previous step
+  auto resolve_step = [&](int j) {
+    cp_async_wait_all();
+    if (j + 3 >= 0 && j + 3 < n) {
+      each([&](int q) { publish_row(sh, j + 3, rrow[q], res_c(a, sh, rb[q], j + 3, rrow[q])); });
+      publish_done(sh, j + 3, lane);
+    }
+    if (j + 4 >= 0 && j + 4 < n) each([&](int q) { res_b(a, sh, ra[q], j + 4, rrow[q], rb[q]); });
+    if (j + 5 >= 0 && j + 5 < n) {
+      each([&](int q) { res_a(a, sh, rc, j + 5, rrow[q], ra[q]); });
+      rc.next(a);
+    }
+    cp_async_commit();
+  };
+  // prologue: tiles 0-2 published, phase B of tile 3 and phase A of tile 4 issued
+  if (nres > 0) {
+#pragma unroll 1
+    for (int j = -5; j < 0; ++j) resolve_step(j);
   }
 
-  for (int j = 0; j < n; ++j) {
-    const TileRef tr = tile_ref(a, lo, n, j);
-    if (!wait_bar_w(sh, sh.bar(kBarRow + (j & 3)), (j >> 2) & 1)) return;
-    const bool valid = sh.rowoff[(j & 3) * 128 + tid] >= 0;
+  if (warp == kIssueWarp && !mma_issue_first<NH>(sh, tmem, lane == 0)) return;
+
+  Cursor cur;
+  cur.init(a, lo);
+  for (int j = 0; j < n; ++j, cur.next(a)) {
+    const bool first = cur.tile == 0 || j == 0;
+    const bool last = cur.tile == a.tiles_per_item - 1 || j == n - 1;
+    const bool valid = sh.rowoff[(j & 3) * kTile + tid] >= 0;
     if (!wait_bar_w(sh, sh.bar(kBarSFull), j & 1)) return;
     tc_fence_after();
-    if (tr.first && tid < 64) sh.m_run[tid] = -INFINITY;
-    // vote slot of the next tile: every read of it (tile j-1) happened before this tile began
-    if (tid == 0) sh.vote[(j + 1) & 1] = 0;
-
-    // ---- optimistic pass: P with the running maxima. Needs a redo only when some score
-    // exceeds its head's maximum by more than 2^8 (always on the first tile of an item).
-    bool need_max = tr.first;
-    if (!need_max) {
-      bool over = false;
-#pragma unroll 1
-      for (int c0 = 0; c0 < NH; c0 += 16) over |= softmax_chunk<NH>(a, sh, tmem + lb + TC::kS + c0, pt, c0, valid, tid);
-      if (__any_sync(0xffffffffu, over) && lane == 0) sh.vote[j & 1] = 1;
-      if (!sm_sync(sh, smph)) return;
-      need_max = sh.vote[j & 1] != 0;
-    }
-    if (need_max) {
-      // ---- per-head maximum of the tile, new running maxima and rescale factors
-#pragma unroll 1
-      for (int c0 = 0; c0 < NH; c0 += CW) {
-        float s[CW];
-#pragma unroll
-        for (int c = 0; c < CW; c += 16) tmem_ld16(tmem + lb + TC::kS + c0 + c, s + c);
-#pragma unroll
-        for (int h = 0; h < CW; ++h) s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
-        warp_col_reduce_store<CW, true>(s, lane, sh.red + warp * 64 + c0);
-      }
-      if (!sm_sync(sh, smph)) return;
-      if (warp == 0) {
-        bool raised = false;
-        for (int h = lane; h < NH; h += 32) {
-          const float tmax = fmaxf(fmaxf(sh.red[h], sh.red[64 + h]), fmaxf(sh.red[128 + h], sh.red[192 + h]));
-          const float mo = sh.m_run[h];
-          float al = 1.f;
-          if (tmax > mo + kLazyRescaleLog2) {
-            al = (mo == -INFINITY) ? 0.f : ex2(mo - tmax);
-            sh.m_run[h] = tmax;
-            raised = true;
-          }
-          sh.alpha[h] = al;
-        }
-        raised = __any_sync(0xffffffffu, raised);
-        if (lane == 0) *sh.rescale_flag = raised ? 1 : 0;
-      }
-      if (!sm_sync(sh, smph)) return;
-#pragma unroll 1
-      for (int c0 = 0; c0 < NH; c0 += 16) softmax_chunk<NH>(a, sh, tmem + lb + TC::kS + c0, pt, c0, valid, tid);
-      // O^T and the row sums *= alpha when a running max moved (the previous PV is complete:
-      // S^T of this tile was committed after it)
-      if (!tr.first && *sh.rescale_flag != 0) {
-#pragma unroll 1
-        for (int b = 0; b <= 4; ++b) {
-          const uint32_t col = b < 4 ? TC::kO + b * NH : TC::kL;
-#pragma unroll 1
-          for (int c0 = 0; c0 < NH; c0 += 16) {
-            float o[16];
-            const uint32_t addr = tmem + lb + col + c0;
-            tmem_ld16(addr, o);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= sh.alpha[c0 + i];
-            tmem_st16(addr, o);
-          }
-        }
-        tmem_st_wait();
-      }
+    // the first tile of an item has no running maxima yet: it always takes the max pass
+    if (!first) {
+      const bool over = p_pass<NH>(a, sh, tl + TC::kS, pt, valid, tid);
+      if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[j & 1] = 1;
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(sh.bar(kBarPReady));
-    if (warp == kIssueWarp) {
-      bool ok = true;
-      if (issuer) ok = mma_issue_after<NH>(a, sh, md, tmem, lo, n, j);
-      __syncwarp();
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-    }
 
-    if (!tr.last) continue;
+    // ---- decision: the issuing thread reads the overflow flag once all four warps arrived (the
+    // first tile of an item always takes the max pass)
+    bool fix;
+    if (warp == kIssueWarp) {
+      if (!wait_bar_w(sh, sh.bar(kBarPReady), j & 1)) return;
+      int f = 0;
+      if (lane == 0) {
+        f = first ? 1 : sh.overflow[j & 1];
+        sh.overflow[j & 1] = 0;
+        sh.decision[j & 1] = f;
+        mbar_arrive(sh.bar(kBarDecision));
+      }
+      fix = __shfl_sync(0xffffffffu, f, 0) != 0;
+    } else {
+      resolve_step(j);
+      if (!wait_bar_w(sh, sh.bar(kBarDecision), j & 1)) return;
+      fix = sh.decision[j & 1] != 0;
+    }
+    if (fix) {
+      if (!max_pass<NH>(a, sh, tl, pt, valid, first, smph, tid)) return;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sh.bar(kBarPFixed));
+    }
+    if (warp == kIssueWarp) {
+      if (fix && !wait_bar_w(sh, sh.bar(kBarPFixed), nfix & 1)) return;
+      if (!mma_issue_after<NH>(sh, tmem, j, n, first, lane == 0)) return;
+    }
+    if (fix) ++nfix;
+
+    if (!last) continue;
     // ---- epilogue of the item segment: wait for its last PV (and row sums)
     if (!wait_bar_w(sh, sh.bar(kBarPvDone + 3), j & 1)) return;
     tc_fence_after();
-    const long long item = tr.item;
-    const int t = static_cast<int>(item / a.groups);
-    const int h0 = static_cast<int>(item - static_cast<long long>(t) * a.groups) * a.heads_per_group;
+    const uint32_t t = item_token(a, cur.item);
+    const int h0 = item_head0(a, cur.item);
     const int hg = min(a.heads_per_group, a.H - h0);
-    const int slot =
-        a.split ? static_cast<int>(blockIdx.x - split_owner(item * a.tiles_per_item, a.total_tiles, a.nctas)) : 0;
-    // thread h (< NH) turns the row sum of head h into the output factor and the LSE
-#pragma unroll 1
-    for (int c0 = 0; c0 < NH; c0 += 16) {
+    const int slot = a.split ? static_cast<int>(blockIdx.x - split_owner(static_cast<long long>(cur.item) *
+                                                                                 a.tiles_per_item,
+                                                                             a.total_tiles, a.nctas))
+                             : 0;
+    // warp w reads the row sums of heads 16w..16w+15 (every lane holds the same sums); lane
+    // i < 16 turns head 16w+i's sum into the output factor and the LSE
+    if (warp * 16 < NH) {
       float l[16];
-      tmem_ld16(tmem + lb + TC::kL + c0, l);
-      if (tid >= c0 && tid < c0 + 16) {
-        const int h = tid;
-        float lh = 0.f;
+      tmem_load<16>(tl + TC::kL + warp * 16, l);
+      if (lane < 16) {
+        const int h = warp * 16 + lane;
+        float lh = l[0];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) lh = (i == tid - c0) ? l[i] : lh;
+        for (int i = 1; i < 16; ++i) lh = (i == lane) ? l[i] : lh;
         const float m = sh.m_run[h];
         float factor = 0.f, lse2 = -INFINITY;
         if (lh > 0.f) {
@@ -807,28 +907,26 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < NH; c0 += 16) {
-        float o[16], f[16];
-        tmem_ld16(tmem + lb + TC::kO + b * NH + c0, o);
+      for (int c0 = 0; c0 < NH; c0 += CW) {
+        float o[CW];
+        tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = sh.fin[c0 + i];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < CW; ++i) {
           const int h = c0 + i;
           if (h < hg) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(f[i] != 0.f ? o[i] * f[i] : 0.f);
+            const float f = sh.fin[h];
+            const __nv_bfloat16 v = __float2bfloat16_rn(f != 0.f ? o[i] * f : 0.f);
             obase[h * hstride + b * 128 + tid] = *reinterpret_cast<const uint16_t*>(&v);
           }
         }
       }
     }
     tc_fence_before();
-    if (!sm_sync(sh, smph)) return;
   }
 }
 
-template <int NH>
-__global__ void __maxnreg__(96) sparse_mla_kernel(const AttnArgs a) {
+template <int NH, int F0, int F1>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ AttnArgs a) {
   using L = Smem<NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -838,14 +936,19 @@ __global__ void __maxnreg__(96) sparse_mla_kernel(const AttnArgs a) {
   sh.q = smem_u32(base + L::kQOff);
   sh.red = reinterpret_cast<float*>(base + L::kRedOff);
   sh.m_run = reinterpret_cast<float*>(base + L::kMOff);
+  sh.m_use = reinterpret_cast<float*>(base + L::kMUseOff);
+  sh.thr = reinterpret_cast<float*>(base + L::kThrOff);
   sh.alpha = reinterpret_cast<float*>(base + L::kAlphaOff);
   sh.fin = reinterpret_cast<float*>(base + L::kFinOff);
-  sh.rowoff = reinterpret_cast<int64_t*>(base + L::kRowOff);
+  sh.rowoff = reinterpret_cast<int32_t*>(base + L::kRowOff);
+  sh.res = smem_u32(base + L::kResOff);
+  sh.resp = reinterpret_cast<int32_t*>(base + L::kResOff);
   sh.bars = smem_u32(base + L::kBarOff);
   sh.tmem_slot = reinterpret_cast<uint32_t*>(base + L::kMiscOff);
   sh.abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
   sh.rescale_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 8);
-  sh.vote = reinterpret_cast<volatile int*>(base + L::kMiscOff + 16);
+  sh.overflow = reinterpret_cast<volatile int*>(base + L::kMiscOff + 16);
+  sh.decision = reinterpret_cast<volatile int*>(base + L::kMiscOff + 24);
   sh.ones = smem_u32(base + L::kOnesOff);
 
   const int warp = threadIdx.x >> 5;
@@ -860,16 +963,19 @@ __global__ void __maxnreg__(96) sparse_mla_kernel(const AttnArgs a) {
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 9; ++i) mbar_init(sh.bar(kBarFull + i), kLdWarps);
+    mbar_init(sh.bar(kBarFullA), kLdWarps);
+    mbar_init(sh.bar(kBarFullB), kLdWarps);
     mbar_init(sh.bar(kBarSFull), 1);
     mbar_init(sh.bar(kBarPReady), kSmWarps);
     mbar_init(sh.bar(kBarSm), kSmWarps * 32);
+    mbar_init(sh.bar(kBarDecision), 1);
+    mbar_init(sh.bar(kBarPFixed), kSmWarps);
     for (int i = 0; i < 4; ++i) mbar_init(sh.bar(kBarPvDone + i), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(sh.bar(kBarRow + i), kLdWarps);
+    for (int i = 0; i < 4; ++i) mbar_init(sh.bar(kBarRow + i), kIssueWarp);
     *sh.abort_flag = 0;
     *sh.rescale_flag = 0;
-    sh.vote[0] = 0;
-    sh.vote[1] = 0;
+    sh.overflow[0] = sh.overflow[1] = 0;
+    sh.decision[0] = sh.decision[1] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(base + L::kOnesOff)[threadIdx.x] = 0x3F803F80u;
@@ -886,9 +992,9 @@ __global__ void __maxnreg__(96) sparse_mla_kernel(const AttnArgs a) {
   if (warp < kSmWarps) {
     softmax_role<NH>(a, sh, tmem, lo, n);
   } else {
-    loader_role<NH>(a, sh, lo, n);
-    cp_async_wait_all();
+    loader_role<NH, F0, F1>(a, sh, lo, n);
   }
+  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -966,16 +1072,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a) {
   if (lane == 0 && a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
 }
 
-template <int NH>
+template <int NH, int F0, int F1>
 cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
   const int smem = Smem<NH>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(sparse_mla_kernel<NH, F0, F1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) {
     note_cuda_error(e, "cudaFuncSetAttribute(sparse_mla_kernel, max dynamic shared memory)");
     return e;
   }
   if (ev0) cudaEventRecord(ev0, stream);
-  sparse_mla_kernel<NH><<<plan.nctas, kThreads, smem, stream>>>(a);
+  sparse_mla_kernel<NH, F0, F1><<<plan.nctas, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
   if (ev1) cudaEventRecord(ev1, stream);
   if (e != cudaSuccess) {
@@ -991,14 +1098,26 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
   return e;
 }
 
+template <int NH>
+cudaError_t launch_fmt(const AttnArgs& a, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
+  const int f0 = a.set[0].format;
+  const int f1 = a.nsets > 1 ? a.set[1].format : f0;
+  switch (f0 * 2 + f1) {
+    case 0: return launch_nh<NH, 0, 0>(a, plan, stream, ev0, ev1);
+    case 1: return launch_nh<NH, 0, 1>(a, plan, stream, ev0, ev1);
+    case 2: return launch_nh<NH, 1, 0>(a, plan, stream, ev0, ev1);
+    default: return launch_nh<NH, 1, 1>(a, plan, stream, ev0, ev1);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& args, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0,
                              cudaEvent_t ev1) {
   switch (plan.nh) {
-    case 16: return launch_nh<16>(args, plan, stream, ev0, ev1);
-    case 32: return launch_nh<32>(args, plan, stream, ev0, ev1);
-    case 64: return launch_nh<64>(args, plan, stream, ev0, ev1);
+    case 16: return launch_fmt<16>(args, plan, stream, ev0, ev1);
+    case 32: return launch_fmt<32>(args, plan, stream, ev0, ev1);
+    case 64: return launch_fmt<64>(args, plan, stream, ev0, ev1);
     default: return cudaErrorInvalidValue;
   }
 }

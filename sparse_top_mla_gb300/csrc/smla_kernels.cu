@@ -386,11 +386,21 @@ __device__ __forceinline__ void ld_issue_rope(int fmt, const uint8_t* cache, con
   }
 }
 
+// Rows k < kDqAhead of the fp8 block pair in slot S, dequantised into registers ahead of the
+// wait for their store (the other rows are converted after it: registers do not allow more).
+constexpr int kDqAhead = 2;
+template <int S>
+__device__ __forceinline__ void ld_dequant_fp8(const LdData& D, uint4 (&dq)[kDqAhead][2]) {
+#pragma unroll
+  for (int k = 0; k < kDqAhead; ++k) dequant16(D.d[S][k], D.sc[S][k], dq[k][0], dq[k][1]);
+}
+
 // An fp8 chunk of 16 channels becomes two bf16 chunks of block 2bp + lane8/4. The threads
 // of the second block store their two chunks in the opposite order, so the 8 threads of a
 // store phase always hit 8 different 16-byte bank groups.
 template <int S>
-__device__ __forceinline__ void ld_store_fp8(const Shared& sh, int rg, int lane8, int bp, const LdData& D) {
+__device__ __forceinline__ void ld_store_fp8(const Shared& sh, int rg, int lane8, int bp, const LdData& D,
+                                             const uint4 (&dq)[kDqAhead][2]) {
   const bool second = (lane8 >> 2) != 0;
   const uint32_t blk = sh.tile + (2 * bp + (lane8 >> 2)) * kBlockBytes;
   const int c0 = (lane8 & 3) * 2;
@@ -398,7 +408,12 @@ __device__ __forceinline__ void ld_store_fp8(const Shared& sh, int rg, int lane8
   for (int k = 0; k < kLdRows; ++k) {
     const int r = rg + 32 * k;
     uint4 lo, hi;
-    dequant16(D.d[S][k], D.sc[S][k], lo, hi);
+    if (k < kDqAhead) {
+      lo = dq[k < kDqAhead ? k : 0][0];
+      hi = dq[k < kDqAhead ? k : 0][1];
+    } else {
+      dequant16(D.d[S][k], D.sc[S][k], lo, hi);
+    }
     sts_v4(blk + swz(r, c0 + (second ? 1 : 0)), second ? hi : lo);
     sts_v4(blk + swz(r, c0 + (second ? 0 : 1)), second ? lo : hi);
   }
@@ -477,6 +492,21 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
 
   auto fmt_of = [&](const Cursor& c) { return F0 == F1 ? F0 : (set_of(a, c.tile) ? F1 : F0); };
   auto cache_of = [&](const Cursor& c) { return SET_FIELD(a, set_of(a, c.tile), cache); };
+  // Whole rows of tile jt into L2, one bulk prefetch per row, two tiles ahead of their loads:
+  // the loads then hit L2, and DRAM serves each gathered row as one contiguous read instead of
+  // one access per 128-byte block pair.
+  auto prefetch_rows = [&](int jt, const Cursor& c) -> bool {
+    int64_t off[kLdRows];
+    if (!get_off(jt, c, off)) return false;
+    if (lane8 == 0) {
+      const uint8_t* cache = cache_of(c);
+      const uint32_t bytes = fmt_of(c) == 1 ? kRowFp8 : kRowBf16;
+#pragma unroll
+      for (int k = 0; k < kLdRows; ++k)
+        if (off[k] >= 0) prefetch_l2_bulk(cache + off[k], bytes);
+    }
+    return true;
+  };
 
   Cursor cur;
   cur.init(a, lo);
@@ -484,6 +514,11 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   int64_t off_cur[kLdRows], off_nxt[kLdRows];
   prefetch_q(cur.item);
   if (!get_off(0, cur, off_cur)) return;
+  if (n > 1) {
+    Cursor c1 = cur;
+    c1.next(a);
+    if (!prefetch_rows(1, c1)) return;
+  }
   {
     const uint8_t* cache = cache_of(cur);
     if (fmt_of(cur) == 1) {
@@ -507,16 +542,25 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       if (nxt.tile == 0) prefetch_q(nxt.item);
       if (!get_off(j + 1, nxt, off_nxt)) return;
     }
+    if (j + 2 < n) {
+      Cursor c2 = nxt;
+      c2.next(a);
+      if (!prefetch_rows(j + 2, c2)) return;
+    }
     const int fmt_cur = fmt_of(cur);
     const int fmt_nxt = has1 ? fmt_of(nxt) : 0;
     const uint8_t* cache_cur = cache_of(cur);
     const uint8_t* cache_nxt = has1 ? cache_of(nxt) : cache_cur;
+    // fp8: each block pair is dequantised before the wait for its PV release, so only the
+    // shared-memory stores remain on the path from that release to the tensor core
+    uint4 dq[kDqAhead][2];
+    if (fmt_cur == 1) ld_dequant_fp8<0>(D, dq);
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
       if (bp == 0 && first) load_q(cur.item);
       if (fmt_cur == 1) {
-        ld_store_fp8<bp>(sh, rg, lane8, bp, D);
+        ld_store_fp8<bp>(sh, rg, lane8, bp, D, dq);
       } else {
         ld_store_bf16<(bp & 1)>(sh, rg, lane8, bp, D);
       }
@@ -556,6 +600,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
           if (bp == 3) ld_issue_rope(1, cache_nxt, off_nxt, lane8, D);
         }
       }
+      if (fmt_cur == 1 && bp < 3) ld_dequant_fp8<(bp < 3 ? bp + 1 : 3)>(D, dq);
       return true;
     };
     if (!step(std::integral_constant<int, 0>{}) || !step(std::integral_constant<int, 1>{}) ||

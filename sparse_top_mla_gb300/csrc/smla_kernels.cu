@@ -943,25 +943,55 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       }
     }
     if (!sm_sync(sh, smph)) return;
-    // O^T: thread tid holds channel 128b + tid of every head; warps write 64-byte runs
+    // O^T: thread tid holds channel 128b + tid of every head. Within each group of 8 lanes an
+    // 8x8 butterfly transpose (3 shuffle stages) gives every lane 8 consecutive channels of one
+    // head, stored as one 16-byte write (output rows are 16-byte aligned, strides multiples of 8).
     uint16_t* obase = a.split ? static_cast<uint16_t*>(a.part_o) +
                                     ((static_cast<int64_t>(slot) * a.T + t) * a.H + h0) * kDv
                               : a.out + static_cast<int64_t>(t) * a.out_stride_t +
                                     static_cast<int64_t>(h0) * a.out_stride_h;
     const int64_t hstride = a.split ? kDv : a.out_stride_h;
+    const int k8 = lane & 7;
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
 #pragma unroll 1
       for (int c0 = 0; c0 < NH; c0 += CW) {
-        float o[CW];
+        float o[CW], f[CW];
         tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
 #pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          const int h = c0 + i;
+        for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
+#pragma unroll
+        for (int q = 0; q < CW / 8; ++q) {
+          float* x = o + 8 * q;  // heads c0+8q .. c0+8q+7 of this lane's channel
+#pragma unroll
+          for (int d = 4; d >= 1; d >>= 1) {
+            const bool upper = (k8 & d) != 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if ((i & d) == 0) {
+                const float send = upper ? x[i] : x[i + d];
+                const float recv = __shfl_xor_sync(0xffffffffu, send, d);
+                if (upper) {
+                  x[i] = recv;
+                } else {
+                  x[i + d] = recv;
+                }
+              }
+            }
+          }
+          // lane 8g+k now holds head c0+8q+k for channels 32w+8g .. 32w+8g+7
+          const int h = c0 + 8 * q + k8;
           if (h < hg) {
-            const float f = sh.fin[h];
-            const __nv_bfloat16 v = __float2bfloat16_rn(f != 0.f ? o[i] * f : 0.f);
-            obase[h * hstride + b * 128 + tid] = *reinterpret_cast<const uint16_t*>(&v);
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+              w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
       }

@@ -823,9 +823,10 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   // stays free)
   const int nres = warp == 0 ? 2 : (warp < kIssueWarp ? 1 : 0);
   const int rrow[2] = {tid, 3 * 32 + lane};
+  // both rows' state stays in registers: the calls below index it with constants
   auto each = [&](auto&& f) {
-#pragma unroll 1
-    for (int q = 0; q < nres; ++q) f(q);
+    f(std::integral_constant<int, 0>{});
+    if (nres > 1) f(std::integral_constant<int, 1>{});
   };
   Cursor rc;
   rc.init(a, lo);
@@ -836,12 +837,12 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   auto resolve_step = [&](int j) {
     cp_async_wait_all();
     if (j + 3 >= 0 && j + 3 < n) {
-      each([&](int q) { publish_row(sh, j + 3, rrow[q], res_c(a, sh, rb[q], j + 3, rrow[q])); });
+      each([&](auto q) { publish_row(sh, j + 3, rrow[q], res_c(a, sh, rb[q], j + 3, rrow[q])); });
       publish_done(sh, j + 3, lane);
     }
-    if (j + 4 >= 0 && j + 4 < n) each([&](int q) { res_b(a, sh, ra[q], j + 4, rrow[q], rb[q]); });
+    if (j + 4 >= 0 && j + 4 < n) each([&](auto q) { res_b(a, sh, ra[q], j + 4, rrow[q], rb[q]); });
     if (j + 5 >= 0 && j + 5 < n) {
-      each([&](int q) { res_a(a, sh, rc, j + 5, rrow[q], ra[q]); });
+      each([&](auto q) { res_a(a, sh, rc, j + 5, rrow[q], ra[q]); });
       rc.next(a);
     }
     cp_async_commit();

@@ -158,7 +158,8 @@ int ntiles_of(const smla_kv_set& s) { return (s.topk + kTile - 1) / kTile; }
 Plan make_plan(const smla_params* p, bool split_k) {
   Plan pl{};
   pl.groups = (p->H + kMaxGroupHeads - 1) / kMaxGroupHeads;
-  pl.heads_per_group = (p->H + pl.groups - 1) / pl.groups;
+  // a multiple of 8, so every group's first head starts a 16-byte run in the partial layout
+  pl.heads_per_group = (((p->H + pl.groups - 1) / pl.groups) + 7) & ~7;
   pl.nh = pl.heads_per_group <= 16 ? 16 : (pl.heads_per_group <= 32 ? 32 : 64);
   pl.tiles_per_item = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
   pl.n_items = static_cast<long long>(p->T) * pl.groups;
@@ -180,7 +181,9 @@ Plan make_plan(const smla_params* p, bool split_k) {
   pl.workspace_bytes = 0;
   if (pl.split && p->T > 0) {
     const size_t n = static_cast<size_t>(pl.max_slots) * p->T * p->H;
-    pl.part_o_bytes = (n * kDv * sizeof(uint16_t) + 255) & ~static_cast<size_t>(255);
+    const size_t hp = (static_cast<size_t>(p->H) + 7) & ~static_cast<size_t>(7);
+    pl.part_o_bytes = (static_cast<size_t>(pl.max_slots) * p->T * kDv * hp * sizeof(uint16_t) + 255) &
+                      ~static_cast<size_t>(255);
     pl.workspace_bytes = pl.part_o_bytes + ((n * sizeof(float) + 255) & ~static_cast<size_t>(255));
   }
   return pl;
@@ -252,6 +255,7 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
   a.split = pl.split;
   a.nctas = pl.nctas;
   a.max_slots = pl.max_slots;
+  a.hp = (p->H + 7) & ~7;
   a.n_items = pl.n_items;
   a.total_tiles = pl.total_tiles;
   a.scale_log2 = p->sm_scale * 1.4426950408889634f;

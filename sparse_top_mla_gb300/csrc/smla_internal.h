@@ -42,7 +42,7 @@ struct AttnArgs {
   int64_t out_stride_t, out_stride_h;
   float* lse;
   int64_t lse_stride_t;
-  void* part_o;     // bf16 [max_slots, T, H, 512] normalised partial O (split schedule only)
+  void* part_o;     // bf16 [max_slots, T, 512, hp] normalised partial O^T (split schedule only)
   float* part_lse;  // [max_slots, T, H] base-2 log-sum-exp of each partial
   KvSetDev set[2];
   int32_t nsets;
@@ -53,6 +53,7 @@ struct AttnArgs {
   int32_t split;           // 0: whole items per CTA, final outputs; 1: contiguous tile ranges, partials
   int32_t nctas;           // persistent CTAs (grid size)
   int32_t max_slots;       // partial slots per item (split schedule)
+  int32_t hp;              // H rounded up to a multiple of 8 (head stride of the partials)
   int64_t n_items;         // T * groups
   int64_t total_tiles;     // n_items * tiles_per_item
   float scale_log2;        // sm_scale * log2(e)

@@ -440,6 +440,25 @@ __device__ __forceinline__ void ld_issue_fp8_rt(const uint8_t* cache, const int6
   }
 }
 
+// Q of one work item (NH heads x 576 channels, zero rows past the group's heads) -> shared
+// memory in the 128-byte-swizzled K-major layout, by the 256 loader threads (cp.async).
+template <int NH>
+__device__ __forceinline__ void load_q_tile(const AttnArgs& a, const Shared& sh, uint32_t item, int u) {
+  const uint32_t t = item_token(a, item);
+  const int h0 = item_head0(a, item);
+  const int hg = min(a.heads_per_group, a.H - h0);
+  const uint16_t* qb = a.q + static_cast<int64_t>(t) * a.q_stride_t;
+  for (int e = u; e < NH * 72; e += kLdThreads) {
+    const int nrow = e / 72;
+    const int c = e - nrow * 72;
+    const bool live = nrow < hg;
+    const uint16_t* src =
+        qb + (live ? static_cast<int64_t>(h0 + nrow) * a.q_stride_h + (c >> 3) * 64 + (c & 7) * 8 : 0);
+    cp_async16(sh.q + (c >> 3) * NH * 128 + swz(nrow, c & 7), src, live ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
 // F0, F1: cache formats of the main and the extra set (compile-time, so each kernel carries only
 // the load paths it uses).
 template <int NH, int F0, int F1>
@@ -450,21 +469,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   const int rg = u >> 3;
   if (n <= 0) return;
 
-  auto load_q = [&](uint32_t item) {
-    const uint32_t t = item_token(a, item);
-    const int h0 = item_head0(a, item);
-    const int hg = min(a.heads_per_group, a.H - h0);
-    const uint16_t* qb = a.q + static_cast<int64_t>(t) * a.q_stride_t;
-    for (int e = u; e < NH * 72; e += kLdThreads) {
-      const int nrow = e / 72;
-      const int c = e - nrow * 72;
-      const bool live = nrow < hg;
-      const uint16_t* src =
-          qb + (live ? static_cast<int64_t>(h0 + nrow) * a.q_stride_h + (c >> 3) * 64 + (c & 7) * 8 : 0);
-      cp_async16(sh.q + (c >> 3) * NH * 128 + swz(nrow, c & 7), src, live ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
+  auto load_q = [&](uint32_t item) { load_q_tile<NH>(a, sh, item, u); };
   auto prefetch_q = [&](uint32_t item) {
     const uint32_t t = item_token(a, item);
     const int h0 = item_head0(a, item);
@@ -512,13 +517,8 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   cur.init(a, lo);
   LdData D;
   int64_t off_cur[kLdRows], off_nxt[kLdRows];
-  prefetch_q(cur.item);
+  load_q(cur.item);  // the first item's Q, while the first row offsets are being resolved
   if (!get_off(0, cur, off_cur)) return;
-  if (n > 1) {
-    Cursor c1 = cur;
-    c1.next(a);
-    if (!prefetch_rows(1, c1)) return;
-  }
   {
     const uint8_t* cache = cache_of(cur);
     if (fmt_of(cur) == 1) {
@@ -531,6 +531,12 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       ld_issue_bf16<0>(cache, off_cur, lane8, 0, D);
       ld_issue_bf16<1>(cache, off_cur, lane8, 1, D);
     }
+  }
+  // the prefetch of tile 1 goes out after tile 0's own loads
+  if (n > 1) {
+    Cursor c1 = cur;
+    c1.next(a);
+    if (!prefetch_rows(1, c1)) return;
   }
 
   for (int j = 0; j < n; ++j) {
@@ -558,7 +564,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
-      if (bp == 0 && first) load_q(cur.item);
+      if (bp == 0 && first && j > 0) load_q(cur.item);
       if (fmt_cur == 1) {
         ld_store_fp8<bp>(sh, rg, lane8, bp, D, dq);
       } else {
@@ -944,55 +950,85 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       }
     }
     if (!sm_sync(sh, smph)) return;
-    // O^T: thread tid holds channel 128b + tid of every head. Within each group of 8 lanes an
-    // 8x8 butterfly transpose (3 shuffle stages) gives every lane 8 consecutive channels of one
-    // head, stored as one 16-byte write (output rows are 16-byte aligned, strides multiples of 8).
-    uint16_t* obase = a.split ? static_cast<uint16_t*>(a.part_o) +
-                                    ((static_cast<int64_t>(slot) * a.T + t) * a.H + h0) * kDv
-                              : a.out + static_cast<int64_t>(t) * a.out_stride_t +
-                                    static_cast<int64_t>(h0) * a.out_stride_h;
-    const int64_t hstride = a.split ? kDv : a.out_stride_h;
-    const int k8 = lane & 7;
+    if (a.split) {
+      // partial O^T rows: thread tid writes channel 128b + tid of the group's heads as one
+      // contiguous run (heads padded to a multiple of 8 in the workspace layout)
+      uint16_t* prow = static_cast<uint16_t*>(a.part_o) +
+                       ((static_cast<int64_t>(slot) * a.T + t) * kDv + tid) * a.hp + h0;
 #pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
+      for (int b = 0; b < 4; ++b) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < NH; c0 += CW) {
-        float o[CW], f[CW];
-        tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
+        for (int c0 = 0; c0 < NH; c0 += CW) {
+          if (c0 >= hg) break;
+          float o[CW], f[CW];
+          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
 #pragma unroll
-        for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
+          for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
+          uint4* dst = reinterpret_cast<uint4*>(prow + static_cast<int64_t>(b) * 128 * a.hp + c0);
 #pragma unroll
-        for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
+          for (int g8 = 0; g8 < CW / 8; ++g8) {
+            if (c0 + 8 * g8 < hg) {
+              uint32_t w4[4];
 #pragma unroll
-        for (int q = 0; q < CW / 8; ++q) {
-          float* x = o + 8 * q;  // heads c0+8q .. c0+8q+7 of this lane's channel
+              for (int e = 0; e < 4; ++e) {
+                const int i = 8 * g8 + 2 * e;
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(f[i] != 0.f ? o[i] * f[i] : 0.f,
+                                                                f[i + 1] != 0.f ? o[i + 1] * f[i + 1] : 0.f);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+              dst[g8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+    } else {
+      // final O: thread tid holds channel 128b + tid of every head. Within each group of 8 lanes
+      // an 8x8 butterfly transpose (3 shuffle stages) gives every lane 8 consecutive channels of
+      // one head, stored as one 16-byte write (rows 16-byte aligned, strides multiples of 8).
+      uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
+      const int64_t hstride = a.out_stride_h;
+      const int k8 = lane & 7;
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < NH; c0 += CW) {
+          float o[CW], f[CW];
+          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
 #pragma unroll
-          for (int d = 4; d >= 1; d >>= 1) {
-            const bool upper = (k8 & d) != 0;
+          for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if ((i & d) == 0) {
-                const float send = upper ? x[i] : x[i + d];
-                const float recv = __shfl_xor_sync(0xffffffffu, send, d);
-                if (upper) {
-                  x[i] = recv;
-                } else {
-                  x[i + d] = recv;
+          for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
+#pragma unroll
+          for (int q = 0; q < CW / 8; ++q) {
+            float* x = o + 8 * q;  // heads c0+8q .. c0+8q+7 of this lane's channel
+#pragma unroll
+            for (int d = 4; d >= 1; d >>= 1) {
+              const bool upper = (k8 & d) != 0;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if ((i & d) == 0) {
+                  const float send = upper ? x[i] : x[i + d];
+                  const float recv = __shfl_xor_sync(0xffffffffu, send, d);
+                  if (upper) {
+                    x[i] = recv;
+                  } else {
+                    x[i + d] = recv;
+                  }
                 }
               }
             }
-          }
-          // lane 8g+k now holds head c0+8q+k for channels 32w+8g .. 32w+8g+7
-          const int h = c0 + 8 * q + k8;
-          if (h < hg) {
-            uint32_t w4[4];
+            // lane 8g+k now holds head c0+8q+k for channels 32w+8g .. 32w+8g+7
+            const int h = c0 + 8 * q + k8;
+            if (h < hg) {
+              uint32_t w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 bb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-              w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 bb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+                w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+              }
+              *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) =
+                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) =
-                make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
       }
@@ -1079,73 +1115,96 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   }
 }
 
-// Split-K combine: one warp per (token, head). Lanes hold the partials' base-2 LSEs; the
-// max and the sum of weights are warp-shuffle reductions; each lane then accumulates 16 of
-// the 512 channels over the partials, applies the sink and writes bf16 O and natural-log LSE.
-__global__ void __launch_bounds__(256) combine_kernel(const AttnArgs a) {
-  const int wg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wg >= a.T * a.H) return;
-  const int t = wg / a.H;
-  const int h = wg - t * a.H;
+// Split-K combine, one CTA per (token, 32-head chunk). Pass 1: thread i < 32 merges head
+// hbase+i's partial base-2 LSEs into the final LSE, the sink factor and per-slot weights
+// 2^(lse_s - lse) (shared memory). Pass 2: thread i owns channels 2i, 2i+1, reads their partial
+// O^T rows (32 contiguous heads per slot) and accumulates the weighted sum, then writes bf16 O
+// (a warp writes 128 contiguous bytes per head).
+constexpr int kCombineThreads = 256;
+constexpr int kCombineHeads = 32;
+
+__device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int& c0, int& ns) {
   const long long item = static_cast<long long>(t) * a.groups + h / a.heads_per_group;
   const long long x0 = item * a.tiles_per_item;
-  const int c0 = static_cast<int>(split_owner(x0, a.total_tiles, a.nctas));
-  const int ns = static_cast<int>(split_owner(x0 + a.tiles_per_item - 1, a.total_tiles, a.nctas)) - c0 + 1;
-  auto lse_at = [&](int s) { return a.part_lse[(static_cast<int64_t>(s) * a.T + t) * a.H + h]; };
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, lse_at(s));
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  uint16_t* orow = a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h) * a.out_stride_h;
-  if (M == -INFINITY) {
-    reinterpret_cast<uint4*>(orow + lane * 16)[0] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(orow + lane * 16)[1] = make_uint4(0, 0, 0, 0);
-    if (lane == 0 && a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = -INFINITY;
-    return;
+  c0 = static_cast<int>(split_owner(x0, a.total_tiles, a.nctas));
+  ns = static_cast<int>(split_owner(x0 + a.tiles_per_item - 1, a.total_tiles, a.nctas)) - c0 + 1;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnArgs a) {
+  extern __shared__ float wts[];  // [max_slots][kCombineHeads]
+  __shared__ float fac[kCombineHeads];
+  __shared__ int nsh[kCombineHeads];
+  const int t = blockIdx.x;
+  const int hbase = blockIdx.y * kCombineHeads;
+  const int tid = threadIdx.x;
+  const int H = a.H;
+  if (tid < kCombineHeads) {
+    const int h = hbase + tid;
+    int ns = 0;
+    float f = 0.f;
+    if (h < H) {
+      int c0;
+      item_slots(a, t, h, c0, ns);
+      const float* lp = a.part_lse + static_cast<int64_t>(t) * H + h;
+      const int64_t sstride = static_cast<int64_t>(a.T) * H;
+      float M = -INFINITY;
+      for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s * sstride]);
+      float L2 = -INFINITY;
+      if (M != -INFINITY) {
+        float W = 0.f;
+        for (int s = 0; s < ns; ++s) W += exp2f(lp[s * sstride] - M);
+        L2 = M + log2f(W);
+      }
+      for (int s = 0; s < ns; ++s) wts[s * kCombineHeads + tid] = L2 == -INFINITY ? 0.f : exp2f(lp[s * sstride] - L2);
+      if (L2 != -INFINITY) f = a.sink != nullptr ? 1.f / (1.f + exp2f(a.sink[h] * 1.4426950408889634f - L2)) : 1.f;
+      if (a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
+    }
+    for (int s = ns; s < a.max_slots; ++s) wts[s * kCombineHeads + tid] = 0.f;
+    fac[tid] = f;
+    nsh[tid] = ns;
   }
-  float W = 0.f;
-  for (int s = lane; s < ns; s += 32) W += exp2f(lse_at(s) - M);
+  __syncthreads();
+  int nsmax = 0;
+#pragma unroll 1
+  for (int i = 0; i < kCombineHeads; ++i) nsmax = max(nsmax, nsh[i]);
+  const int c = 2 * tid;  // this thread's channels c, c+1
+  float acc[2][kCombineHeads];
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-  const float L2 = M + log2f(W);
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kCombineHeads; ++i) acc[0][i] = acc[1][i] = 0.f;
   const uint16_t* part = static_cast<const uint16_t*>(a.part_o);
-  for (int s0 = 0; s0 < ns; s0 += 32) {
-    const int s = s0 + lane;
-    const float wl = s < ns ? exp2f(lse_at(s) - L2) : 0.f;
-    const int cnt = min(32, ns - s0);
-    for (int k = 0; k < cnt; ++k) {
-      const float w = __shfl_sync(0xffffffffu, wl, k);
-      if (w == 0.f) continue;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          part + ((static_cast<int64_t>(s0 + k) * a.T + t) * a.H + h) * kDv + lane * 16);
+#pragma unroll 1
+  for (int s = 0; s < nsmax; ++s) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint4 v = src[q];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    for (int k = 0; k < 2; ++k) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(part + ((static_cast<int64_t>(s) * a.T + t) * kDv + c + k) * a.hp + hbase);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
-          acc[8 * q + 2 * e] += w * f.x;
-          acc[8 * q + 2 * e + 1] += w * f.y;
+      for (int g = 0; g < kCombineHeads / 8; ++g) {
+        if (hbase + 8 * g < H) {
+          const uint4 v = src[g];
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // slots past a head's own range (weight 0) hold unrelated data: select, not multiply
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+            const int i = 8 * g + 2 * e;
+            const float w0 = wts[s * kCombineHeads + i], w1 = wts[s * kCombineHeads + i + 1];
+            acc[k][i] += w0 != 0.f ? w0 * f.x : 0.f;
+            acc[k][i + 1] += w1 != 0.f ? w1 * f.y : 0.f;
+          }
         }
       }
     }
   }
-  float f = 1.f;
-  if (a.sink != nullptr) f = 1.f / (1.f + exp2f(a.sink[h] * 1.4426950408889634f - L2));
-  uint32_t w32[8];
+  uint16_t* orow = a.out + static_cast<int64_t>(t) * a.out_stride_t + c;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * k] * f, acc[2 * k + 1] * f);
-    w32[k] = *reinterpret_cast<const uint32_t*>(&b);
+  for (int i = 0; i < kCombineHeads; ++i) {
+    const int h = hbase + i;
+    if (h < H) {
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[0][i] * fac[i], acc[1][i] * fac[i]);
+      *reinterpret_cast<__nv_bfloat162*>(orow + static_cast<int64_t>(h) * a.out_stride_h) = bb;
+    }
   }
-  reinterpret_cast<uint4*>(orow + lane * 16)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
-  reinterpret_cast<uint4*>(orow + lane * 16)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
-  if (lane == 0 && a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
 }
 
 template <int NH, int F0, int F1>
@@ -1166,8 +1225,9 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     return e;
   }
   if (plan.split) {
-    const long long warps = static_cast<long long>(a.T) * a.H;
-    combine_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(a);
+    const size_t wbytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
+    combine_kernel<<<dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads), kCombineThreads,
+                     wbytes, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) note_cuda_error(e, "launch of combine_kernel");
   }

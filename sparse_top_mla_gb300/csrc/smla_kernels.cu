@@ -499,11 +499,12 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   auto cache_of = [&](const Cursor& c) { return SET_FIELD(a, set_of(a, c.tile), cache); };
   // Whole rows of tile jt into L2, one bulk prefetch per row, two tiles ahead of their loads:
   // the loads then hit L2, and DRAM serves each gathered row as one contiguous read instead of
-  // one access per 128-byte block pair.
+  // one access per 128-byte block pair. Tiles 1 and 2 are not prefetched: at kernel start every
+  // CTA's first loads already saturate DRAM.
   auto prefetch_rows = [&](int jt, const Cursor& c) -> bool {
     int64_t off[kLdRows];
     if (!get_off(jt, c, off)) return false;
-    if (lane8 == 0) {
+    if (lane8 == 0 && jt >= 3) {
       const uint8_t* cache = cache_of(c);
       const uint32_t bytes = fmt_of(c) == 1 ? kRowFp8 : kRowBf16;
 #pragma unroll
@@ -1113,6 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem, TmemCols<NH>::kAlloc);
   }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Split-K combine, one CTA per (token, 32-head chunk). Pass 1: thread i < 32 merges head
@@ -1134,6 +1136,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   extern __shared__ float wts[];  // [max_slots][kCombineHeads]
   __shared__ float fac[kCombineHeads];
   __shared__ int nsh[kCombineHeads];
+  // launched as a programmatic dependent of the attention kernel: wait for its partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int hbase = blockIdx.y * kCombineHeads;
   const int tid = threadIdx.x;
@@ -1147,15 +1151,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       item_slots(a, t, h, c0, ns);
       const float* lp = a.part_lse + static_cast<int64_t>(t) * H + h;
       const int64_t sstride = static_cast<int64_t>(a.T) * H;
+      // the partial LSEs go to shared memory first (all loads in flight together), then the
+      // max, the sum and the weights are computed from there
+      for (int s = 0; s < ns; ++s) wts[s * kCombineHeads + tid] = lp[s * sstride];
       float M = -INFINITY;
-      for (int s = 0; s < ns; ++s) M = fmaxf(M, lp[s * sstride]);
+      for (int s = 0; s < ns; ++s) M = fmaxf(M, wts[s * kCombineHeads + tid]);
       float L2 = -INFINITY;
       if (M != -INFINITY) {
         float W = 0.f;
-        for (int s = 0; s < ns; ++s) W += exp2f(lp[s * sstride] - M);
+        for (int s = 0; s < ns; ++s) W += exp2f(wts[s * kCombineHeads + tid] - M);
         L2 = M + log2f(W);
       }
-      for (int s = 0; s < ns; ++s) wts[s * kCombineHeads + tid] = L2 == -INFINITY ? 0.f : exp2f(lp[s * sstride] - L2);
+      for (int s = 0; s < ns; ++s)
+        wts[s * kCombineHeads + tid] = L2 == -INFINITY ? 0.f : exp2f(wts[s * kCombineHeads + tid] - L2);
       if (L2 != -INFINITY) f = a.sink != nullptr ? 1.f / (1.f + exp2f(a.sink[h] * 1.4426950408889634f - L2)) : 1.f;
       if (a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
     }
@@ -1167,43 +1175,59 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   int nsmax = 0;
 #pragma unroll 1
   for (int i = 0; i < kCombineHeads; ++i) nsmax = max(nsmax, nsh[i]);
-  const int c = 2 * tid;  // this thread's channels c, c+1
-  float acc[2][kCombineHeads];
+  // pass 2: 16-byte chunk j of a slot's partial block (channel j/4, heads 8(j%4)..+7 of the
+  // chunk) is read by thread j % 256: four consecutive threads read one channel's 64 bytes
+  constexpr int kChunks = kDv * (kCombineHeads / 8) / kCombineThreads;  // 8 per thread
+  const int g = tid & 3;                                                  // head group of this thread
+  float acc[kChunks][8];
 #pragma unroll
-  for (int i = 0; i < kCombineHeads; ++i) acc[0][i] = acc[1][i] = 0.f;
+  for (int q = 0; q < kChunks; ++q)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+  const bool live = hbase + 8 * g < H;
   const uint16_t* part = static_cast<const uint16_t*>(a.part_o);
 #pragma unroll 1
   for (int s = 0; s < nsmax; ++s) {
+    const uint16_t* blk = part + (static_cast<int64_t>(s) * a.T + t) * kDv * a.hp + hbase + 8 * g;
+    float w[8];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(part + ((static_cast<int64_t>(s) * a.T + t) * kDv + c + k) * a.hp + hbase);
+    for (int i = 0; i < 8; ++i) w[i] = wts[s * kCombineHeads + 8 * g + i];
+    uint4 v[kChunks];
 #pragma unroll
-      for (int g = 0; g < kCombineHeads / 8; ++g) {
-        if (hbase + 8 * g < H) {
-          const uint4 v = src[g];
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    for (int q = 0; q < kChunks; ++q) {
+      const int c = (tid >> 2) + q * (kCombineThreads / 4);
+      v[q] = live ? *reinterpret_cast<const uint4*>(blk + static_cast<int64_t>(c) * a.hp) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            // slots past a head's own range (weight 0) hold unrelated data: select, not multiply
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
-            const int i = 8 * g + 2 * e;
-            const float w0 = wts[s * kCombineHeads + i], w1 = wts[s * kCombineHeads + i + 1];
-            acc[k][i] += w0 != 0.f ? w0 * f.x : 0.f;
-            acc[k][i + 1] += w1 != 0.f ? w1 * f.y : 0.f;
-          }
-        }
+    for (int q = 0; q < kChunks; ++q) {
+      const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // slots past a head's own range (weight 0) hold unrelated data: select, not multiply
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+        acc[q][2 * e] += w[2 * e] != 0.f ? w[2 * e] * f.x : 0.f;
+        acc[q][2 * e + 1] += w[2 * e + 1] != 0.f ? w[2 * e + 1] * f.y : 0.f;
       }
     }
   }
-  uint16_t* orow = a.out + static_cast<int64_t>(t) * a.out_stride_t + c;
+  // transpose through shared memory (bf16 [32 heads][512 channels]), then coalesced stores
+  __shared__ __align__(16) uint16_t ot[kCombineHeads][kDv];
 #pragma unroll
-  for (int i = 0; i < kCombineHeads; ++i) {
-    const int h = hbase + i;
-    if (h < H) {
-      const __nv_bfloat162 bb = __floats2bfloat162_rn(acc[0][i] * fac[i], acc[1][i] * fac[i]);
-      *reinterpret_cast<__nv_bfloat162*>(orow + static_cast<int64_t>(h) * a.out_stride_h) = bb;
+  for (int q = 0; q < kChunks; ++q) {
+    const int c = (tid >> 2) + q * (kCombineThreads / 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(acc[q][i] * fac[8 * g + i]);
+      ot[8 * g + i][c] = *reinterpret_cast<const uint16_t*>(&b);
     }
+  }
+  __syncthreads();
+  uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t;
+  for (int e = tid; e < kCombineHeads * (kDv / 8); e += kCombineThreads) {
+    const int hh = e / (kDv / 8), c8 = (e - hh * (kDv / 8)) * 8;
+    if (hbase + hh < H)
+      *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(hbase + hh) * a.out_stride_h + c8) =
+          *reinterpret_cast<const uint4*>(&ot[hh][c8]);
   }
 }
 
@@ -1225,9 +1249,25 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     return e;
   }
   if (plan.split) {
-    const size_t wbytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
-    combine_kernel<<<dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads), kCombineThreads,
-                     wbytes, stream>>>(a);
+    // programmatic dependent launch: the combine grid is scheduled while the attention kernel
+    // drains and waits (griddepcontrol.wait) for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
+    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(cfg.dynamicSmemBytes));
+    if (e != cudaSuccess) {
+      note_cuda_error(e, "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)");
+      return e;
+    }
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) note_cuda_error(e, "launch of combine_kernel");
   }

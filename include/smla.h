@@ -125,8 +125,8 @@ size_t smla_workspace_size(const smla_params* p);
 smla_status smla_prefill(const smla_params* p, smla_stream_t stream);
 
 /* Decode schedule: the index list of each (token, head group) is split across CTAs
- * (split-K); partial outputs go to `workspace` and a combine kernel merges them with a
- * warp-shuffle log-sum-exp reduction, then applies the sink. Correct for any T >= 1.
+ * (split-K); partial outputs go to `workspace` and a combine kernel merges them by their
+ * log-sum-exps, then applies the sink. Correct for any T >= 1.
  * Requires workspace_bytes >= smla_workspace_size(p). (sglang PR Problem: decode, few
  * rows, KV-bandwidth-bound; flashinfer PR "explain ..." merged body: decode split-K.) */
 smla_status smla_decode(const smla_params* p, smla_stream_t stream);

@@ -27,7 +27,7 @@
 //
 // Schedules: whole items per CTA (prefill; the epilogue writes O and LSE), or contiguous
 // flat tile ranges per CTA (split-K decode; every item segment writes a normalised partial
-// O in bf16 and a base-2 partial LSE, merged by combine_kernel with warp shuffles).
+// O in bf16 and a base-2 partial LSE, merged by combine_kernel).
 //
 // Heads ride in the MMA N dimension (16, 32 or 64 per group), so every head count runs
 // without padding memory traffic or outputs; unused N columns are zero Q rows.
@@ -1117,13 +1117,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Split-K combine, one CTA per (token, 32-head chunk). Pass 1: thread i < 32 merges head
-// hbase+i's partial base-2 LSEs into the final LSE, the sink factor and per-slot weights
-// 2^(lse_s - lse) (shared memory). Pass 2: thread i owns channels 2i, 2i+1, reads their partial
-// O^T rows (32 contiguous heads per slot) and accumulates the weighted sum, then writes bf16 O
-// (a warp writes 128 contiguous bytes per head).
+// Split-K combine, one CTA per (token, 32-head chunk, half of the 512 channels). Each thread
+// owns an 8-head subgroup and 4 channels of the half; it issues the loads of its first four
+// partial slots before anything else, so they are in flight while threads 0..31 merge the
+// heads' partial base-2 LSEs into the final LSE, the sink factor and the per-slot weights
+// 2^(lse_s - lse) (shared memory). The weighted sums are transposed through shared memory and
+// written as bf16 O with 16-byte stores.
 constexpr int kCombineThreads = 256;
 constexpr int kCombineHeads = 32;
+constexpr int kCombineHalves = 2;
+constexpr int kCombineCh = kDv / kCombineHalves;  // channels per CTA: 256
+constexpr int kCombineSlots = 4;                  // partial slots loaded per round
 
 __device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int& c0, int& ns) {
   const long long item = static_cast<long long>(t) * a.groups + h / a.heads_per_group;
@@ -1135,86 +1139,103 @@ __device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int&
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ float wts[];  // [max_slots][kCombineHeads]
   __shared__ float fac[kCombineHeads];
-  __shared__ int nsh[kCombineHeads];
+  __shared__ __align__(16) uint16_t ot[kCombineHeads][kCombineCh];
   // launched as a programmatic dependent of the attention kernel: wait for its partials
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int hbase = blockIdx.y * kCombineHeads;
+  const int cbase = blockIdx.z * kCombineCh;
   const int tid = threadIdx.x;
   const int H = a.H;
+
+  // 16-byte chunk (channel cbase + tid/4 + 64q, heads hbase + 8g .. +7) of every slot's
+  // partial block: four consecutive threads read one channel's 64 contiguous bytes
+  constexpr int kChunks = kCombineCh * (kCombineHeads / 8) / kCombineThreads;  // 4
+  constexpr int kChStep = kCombineThreads / 4;
+  const int g = tid & 3;
+  int ns = 0;  // slots of this thread's 8 heads (heads_per_group is a multiple of 8)
+  if (hbase + 8 * g < H) {
+    int c0;
+    item_slots(a, t, hbase + 8 * g, c0, ns);
+  }
+  const int64_t sstride = static_cast<int64_t>(a.T) * kDv * a.hp;
+  const uint16_t* col = static_cast<const uint16_t*>(a.part_o) +
+                        (static_cast<int64_t>(t) * kDv + cbase + (tid >> 2)) * a.hp + hbase + 8 * g;
+  uint4 v[kCombineSlots][kChunks];
+  auto issue = [&](int s0) {
+#pragma unroll
+    for (int s = 0; s < kCombineSlots; ++s)
+#pragma unroll
+      for (int q = 0; q < kChunks; ++q)
+        v[s][q] = s0 + s < ns ? *reinterpret_cast<const uint4*>(col + (s0 + s) * sstride +
+                                                                 static_cast<int64_t>(q) * kChStep * a.hp)
+                              : make_uint4(0, 0, 0, 0);
+  };
+  issue(0);
+
   if (tid < kCombineHeads) {
     const int h = hbase + tid;
-    int ns = 0;
+    int nh = 0;
     float f = 0.f;
     if (h < H) {
       int c0;
-      item_slots(a, t, h, c0, ns);
+      item_slots(a, t, h, c0, nh);
       const float* lp = a.part_lse + static_cast<int64_t>(t) * H + h;
-      const int64_t sstride = static_cast<int64_t>(a.T) * H;
+      const int64_t lstride = static_cast<int64_t>(a.T) * H;
       // the partial LSEs go to shared memory first (all loads in flight together), then the
       // max, the sum and the weights are computed from there
-      for (int s = 0; s < ns; ++s) wts[s * kCombineHeads + tid] = lp[s * sstride];
+      for (int s = 0; s < nh; ++s) wts[s * kCombineHeads + tid] = lp[s * lstride];
       float M = -INFINITY;
-      for (int s = 0; s < ns; ++s) M = fmaxf(M, wts[s * kCombineHeads + tid]);
+      for (int s = 0; s < nh; ++s) M = fmaxf(M, wts[s * kCombineHeads + tid]);
       float L2 = -INFINITY;
       if (M != -INFINITY) {
         float W = 0.f;
-        for (int s = 0; s < ns; ++s) W += exp2f(wts[s * kCombineHeads + tid] - M);
+        for (int s = 0; s < nh; ++s) W += exp2f(wts[s * kCombineHeads + tid] - M);
         L2 = M + log2f(W);
       }
-      for (int s = 0; s < ns; ++s)
+      for (int s = 0; s < nh; ++s)
         wts[s * kCombineHeads + tid] = L2 == -INFINITY ? 0.f : exp2f(wts[s * kCombineHeads + tid] - L2);
       if (L2 != -INFINITY) f = a.sink != nullptr ? 1.f / (1.f + exp2f(a.sink[h] * 1.4426950408889634f - L2)) : 1.f;
-      if (a.lse != nullptr) a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
+      if (a.lse != nullptr && blockIdx.z == 0)
+        a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
     }
-    for (int s = ns; s < a.max_slots; ++s) wts[s * kCombineHeads + tid] = 0.f;
+    for (int s = nh; s < a.max_slots; ++s) wts[s * kCombineHeads + tid] = 0.f;
     fac[tid] = f;
-    nsh[tid] = ns;
   }
   __syncthreads();
-  int nsmax = 0;
-#pragma unroll 1
-  for (int i = 0; i < kCombineHeads; ++i) nsmax = max(nsmax, nsh[i]);
-  // pass 2: 16-byte chunk j of a slot's partial block (channel j/4, heads 8(j%4)..+7 of the
-  // chunk) is read by thread j % 256: four consecutive threads read one channel's 64 bytes
-  constexpr int kChunks = kDv * (kCombineHeads / 8) / kCombineThreads;  // 8 per thread
-  const int g = tid & 3;                                                  // head group of this thread
+
   float acc[kChunks][8];
 #pragma unroll
   for (int q = 0; q < kChunks; ++q)
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
-  const bool live = hbase + 8 * g < H;
-  const uint16_t* part = static_cast<const uint16_t*>(a.part_o);
 #pragma unroll 1
-  for (int s = 0; s < nsmax; ++s) {
-    const uint16_t* blk = part + (static_cast<int64_t>(s) * a.T + t) * kDv * a.hp + hbase + 8 * g;
-    float w[8];
+  for (int s0 = 0; s0 < ns; s0 += kCombineSlots) {
+    if (s0 > 0) issue(s0);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = wts[s * kCombineHeads + 8 * g + i];
-    uint4 v[kChunks];
+    for (int s = 0; s < kCombineSlots; ++s) {
+      if (s0 + s >= ns) break;
+      float w[8];
 #pragma unroll
-    for (int q = 0; q < kChunks; ++q) {
-      const int c = (tid >> 2) + q * (kCombineThreads / 4);
-      v[q] = live ? *reinterpret_cast<const uint4*>(blk + static_cast<int64_t>(c) * a.hp) : make_uint4(0, 0, 0, 0);
-    }
+      for (int i = 0; i < 8; ++i) w[i] = wts[(s0 + s) * kCombineHeads + 8 * g + i];
 #pragma unroll
-    for (int q = 0; q < kChunks; ++q) {
-      const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+      for (int q = 0; q < kChunks; ++q) {
+        const uint32_t wv[4] = {v[s][q].x, v[s][q].y, v[s][q].z, v[s][q].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // slots past a head's own range (weight 0) hold unrelated data: select, not multiply
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
-        acc[q][2 * e] += w[2 * e] != 0.f ? w[2 * e] * f.x : 0.f;
-        acc[q][2 * e + 1] += w[2 * e + 1] != 0.f ? w[2 * e + 1] * f.y : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          // a slot past one head's own range (weight 0) may hold unrelated data: select, not
+          // multiply
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+          acc[q][2 * e] += w[2 * e] != 0.f ? w[2 * e] * f.x : 0.f;
+          acc[q][2 * e + 1] += w[2 * e + 1] != 0.f ? w[2 * e + 1] * f.y : 0.f;
+        }
       }
     }
   }
-  // transpose through shared memory (bf16 [32 heads][512 channels]), then coalesced stores
-  __shared__ __align__(16) uint16_t ot[kCombineHeads][kDv];
+  // transpose through shared memory (bf16 [32 heads][256 channels]), then coalesced stores
 #pragma unroll
   for (int q = 0; q < kChunks; ++q) {
-    const int c = (tid >> 2) + q * (kCombineThreads / 4);
+    const int c = (tid >> 2) + q * kChStep;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const __nv_bfloat16 b = __float2bfloat16_rn(acc[q][i] * fac[8 * g + i]);
@@ -1222,9 +1243,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     }
   }
   __syncthreads();
-  uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t;
-  for (int e = tid; e < kCombineHeads * (kDv / 8); e += kCombineThreads) {
-    const int hh = e / (kDv / 8), c8 = (e - hh * (kDv / 8)) * 8;
+  uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t + cbase;
+#pragma unroll
+  for (int e = tid; e < kCombineHeads * (kCombineCh / 8); e += kCombineThreads) {
+    const int hh = e / (kCombineCh / 8), c8 = (e - hh * (kCombineCh / 8)) * 8;
     if (hbase + hh < H)
       *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(hbase + hh) * a.out_stride_h + c8) =
           *reinterpret_cast<const uint4*>(&ot[hh][c8]);
@@ -1252,7 +1274,7 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     // programmatic dependent launch: the combine grid is scheduled while the attention kernel
     // drains and waits (griddepcontrol.wait) for its results
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads, kCombineHalves);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
     e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1268,7 +1290,7 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) note_cuda_error(e, "launch of combine_kernel");
   }
   return e;

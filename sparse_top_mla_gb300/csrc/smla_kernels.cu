@@ -637,15 +637,15 @@ __device__ __forceinline__ MmaDesc make_descs(const Shared& sh) {
   return d;
 }
 
-// The whole issuing warp runs the issue code (waits are warp-wide); only its lane 0 issues the
-// MMAs and commits, as predicated instructions. A warp whose lanes stay diverged for the length
+// The whole issuing warp runs the issue code (waits are warp-wide); elect.sync inside each MMA
+// and commit picks the one lane that issues. A warp whose lanes stay diverged for the length
 // of an issue sequence pays several hundred cycles to reconverge afterwards.
 //
 // QK^T of tile j, waiting once for blocks 0-3 and once for blocks 4-8 (every mbarrier wait in
 // the issue stream lets the tensor pipe run dry for a few hundred cycles). Fully unrolled: in
 // a loop the advancing descriptors cost ~40 cycles per MMA.
 template <int NH>
-__device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint32_t tmem, int j, bool leader) {
+__device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint32_t tmem, int j) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 0);
 #pragma unroll
   for (int kb = 0; kb < kKBlocks; ++kb) {
@@ -655,8 +655,8 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
     }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      mma_bf16_ss(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint64_t>((kb * kBlockBytes + ks * 32) >> 4),
-                  d.qk_b + static_cast<uint64_t>((kb * NH * 128 + ks * 32) >> 4), idesc, (kb | ks) != 0, leader);
+      mma_bf16_ss_warp(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint64_t>((kb * kBlockBytes + ks * 32) >> 4),
+                       d.qk_b + static_cast<uint64_t>((kb * NH * 128 + ks * 32) >> 4), idesc, (kb | ks) != 0);
   }
   return true;
 }
@@ -664,35 +664,34 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
 // O^T block pair bp (value channels 128bp..128bp+127) += V^T . P^T, then a commit that releases
 // the tile's blocks 2bp, 2bp+1 to the loaders.
 template <int NH>
-__device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint32_t tmem, int bp, bool first,
-                                       bool leader) {
+__device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint32_t tmem, int bp, bool first) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 1, 1);
   const uint64_t da = d.pv_a + static_cast<uint64_t>((2 * bp * kBlockBytes) >> 4);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
-    mma_bf16_ss(tmem + TmemCols<NH>::kO + bp * NH, da + static_cast<uint64_t>((ks * 2048) >> 4),
-                d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc, (first && ks == 0) ? 0u : 1u, leader);
-  mma_commit(sh.bar(kBarPvDone + bp), leader);
+    mma_bf16_ss_warp(tmem + TmemCols<NH>::kO + bp * NH, da + static_cast<uint64_t>((ks * 2048) >> 4),
+                     d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc, (first && ks == 0) ? 0u : 1u);
+  mma_commit_warp(sh.bar(kBarPvDone + bp));
 }
 
 // Row sums of P for every head: L[m, h] += sum_k 1 * P^T[k, h] (all 128 lanes get the same
 // sums). Same B operand and accumulate rule as PV, so the normalisation uses exactly the bf16
 // P that multiplied V.
 template <int NH>
-__device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first, bool leader) {
+__device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 1);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
-    mma_bf16_ss(tmem + TmemCols<NH>::kL, d.ones, d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc,
-                (first && ks == 0) ? 0u : 1u, leader);
+    mma_bf16_ss_warp(tmem + TmemCols<NH>::kL, d.ones, d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc,
+                     (first && ks == 0) ? 0u : 1u);
 }
 
 // QK^T of the first tile of the stream.
 template <int NH>
-__device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem, bool leader) {
+__device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem) {
   const MmaDesc d = make_descs<NH>(sh);
-  if (!mma_qk<NH>(sh, d, tmem, 0, leader)) return false;
-  mma_commit(sh.bar(kBarSFull), leader);
+  if (!mma_qk<NH>(sh, d, tmem, 0)) return false;
+  mma_commit_warp(sh.bar(kBarSFull));
   return true;
 }
 
@@ -700,18 +699,17 @@ __device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem,
 // loaders refill a block pair as soon as it is released) and the row sums (before the last
 // block pair, so its commit covers them), then QK^T of tile j+1 as its blocks arrive.
 template <int NH>
-__device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem, int j, int n, bool first,
-                                                bool leader) {
+__device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem, int j, int n, bool first) {
   const MmaDesc d = make_descs<NH>(sh);
   tc_fence_after();
 #pragma unroll 1
   for (int bp = 0; bp < 4; ++bp) {
-    if (bp == 3) mma_rowsum<NH>(d, tmem, first, leader);
-    mma_pv<NH>(sh, d, tmem, bp, first, leader);
+    if (bp == 3) mma_rowsum<NH>(d, tmem, first);
+    mma_pv<NH>(sh, d, tmem, bp, first);
   }
   if (j + 1 >= n) return true;
-  if (!mma_qk<NH>(sh, d, tmem, j + 1, leader)) return false;
-  mma_commit(sh.bar(kBarSFull), leader);
+  if (!mma_qk<NH>(sh, d, tmem, j + 1)) return false;
+  mma_commit_warp(sh.bar(kBarSFull));
   return true;
 }
 
@@ -860,13 +858,18 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     for (int j = -5; j < 0; ++j) resolve_step(j);
   }
 
-  if (warp == kIssueWarp && !mma_issue_first<NH>(sh, tmem, lane == 0)) return;
+  if (warp == kIssueWarp && !mma_issue_first<NH>(sh, tmem)) return;
 
   Cursor cur;
   cur.init(a, lo);
   for (int j = 0; j < n; ++j, cur.next(a)) {
     const bool first = cur.tile == 0 || j == 0;
     const bool last = cur.tile == a.tiles_per_item - 1 || j == n - 1;
+    // resolution runs while QK^T of tile j is in flight, so tile j+3's rows are published before
+    // the loaders look for them at the start of their next tile. It reuses the row slot of tile
+    // j-1, whose readers (the loaders, two and three tiles earlier) finished before that tile's
+    // S^T was ready.
+    if (warp != kIssueWarp) resolve_step(j);
     const bool valid = sh.rowoff[(j & 3) * kTile + tid] >= 0;
     if (!wait_bar_w(sh, sh.bar(kBarSFull), j & 1)) return;
     tc_fence_after();
@@ -894,7 +897,6 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       }
       fix = __shfl_sync(0xffffffffu, f, 0) != 0;
     } else {
-      resolve_step(j);
       if (!wait_bar_w(sh, sh.bar(kBarDecision), j & 1)) return;
       fix = sh.decision[j & 1] != 0;
     }
@@ -907,7 +909,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     }
     if (warp == kIssueWarp) {
       if (fix && !wait_bar_w(sh, sh.bar(kBarPFixed), nfix & 1)) return;
-      if (!mma_issue_after<NH>(sh, tmem, j, n, first, lane == 0)) return;
+      if (!mma_issue_after<NH>(sh, tmem, j, n, first)) return;
     }
     if (fix) ++nfix;
 

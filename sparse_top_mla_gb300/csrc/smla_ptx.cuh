@@ -136,6 +136,25 @@ __device__ __forceinline__ void mma_commit(uint32_t bar, bool issue = true) {
       : "memory");
 }
 
+// Warp-collective forms of the two above: every lane of the converged warp executes them and
+// elect.sync picks the issuing lane (the same lane for every call of a converged warp, so a
+// commit tracks the MMAs issued before it). Measured on GB300 with a 76-MMA tile sequence
+// (M = 128, N = 64): ~52 cycles per MMA, against ~68 with a lane-0 predicate.
+__device__ __forceinline__ void mma_bf16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b32 r;\n elect.sync r|q, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred q;\n .reg .b32 r;\n elect.sync r|q, 0xffffffff;\n"
+      " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
+
 // 32 lanes x 16 columns of 32-bit (each thread: its lane, 16 consecutive columns), then wait.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];

@@ -1103,6 +1103,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot;
+  // launched as a programmatic dependent of the previous kernel on the stream: the set-up above
+  // overlaps its tail; nothing in global memory is read or written before it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp < kSmWarps) {
     softmax_role<NH>(a, sh, tmem, lo, n);
@@ -1264,9 +1267,23 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     note_cuda_error(e, "cudaFuncSetAttribute(sparse_mla_kernel, max dynamic shared memory)");
     return e;
   }
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
   if (ev0) cudaEventRecord(ev0, stream);
-  sparse_mla_kernel<NH, F0, F1><<<plan.nctas, kThreads, smem, stream>>>(a);
-  e = cudaGetLastError();
+  {
+    // programmatic dependent launch: the grid is scheduled while the previous kernel on the
+    // stream drains; the kernel waits for it (griddepcontrol.wait) before touching memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.nctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sparse_mla_kernel<NH, F0, F1>, a);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   if (ev1) cudaEventRecord(ev1, stream);
   if (e != cudaSuccess) {
     note_cuda_error(e, "launch of sparse_mla_kernel");
@@ -1286,10 +1303,7 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
       return e;
     }
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
+    cfg.attrs = &pdl;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
     if (e == cudaSuccess) e = cudaGetLastError();

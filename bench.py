@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny"])
     ap.add_argument("--extra-lines", action="store_true",
                     help="also print one JSON line per secondary workload to stderr")
     return ap.parse_args()
@@ -95,6 +95,8 @@ def build_workloads(kind):
         return rots, "decode fp8: 64 seqs x 16384 ctx (688 MB cache), T=64, H=64, topk=2048 (5% -1), sink"
     if kind == "prefill":
         return [synth.config(3)], "prefill bf16: 1 seq x 32768 ctx, T=4096, H=32, topk=512 causal, sink"
+    if kind == "tiny":
+        return [synth.config(1)], "tiny bf16: 1 seq x 256 ctx, T=4, H=16, topk=128, no sink"
     return [synth.config(4)], ("large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T=8192, H=128, "
                                "topk=2048 causal + 128-token window, sink")
 
@@ -197,10 +199,10 @@ def run_reference(args, world, rank):
     import oracle
     from sparse_top_mla_gb300 import synth
     oracle.build()
-    w = synth.config(2) if args.workload == "decode" else (synth.config(3) if args.workload == "prefill"
-                                                             else synth.config(4, T=64))
+    w = {"decode": lambda: synth.config(2), "prefill": lambda: synth.config(3), "tiny": lambda: synth.config(1),
+         "large_prefill": lambda: synth.config(4, T=64)}[args.workload]()
     per_tok = w.gathered_bytes() / w.T
-    n_tok = {"decode": 64, "prefill": 256, "large_prefill": 16}[args.workload]
+    n_tok = {"decode": 64, "prefill": 256, "large_prefill": 16, "tiny": 4}[args.workload]
     threads = oracle.threads(0)
     times = []
     for s in range(args.warmup + args.steps):
@@ -355,12 +357,13 @@ def cpu_baseline_decode():
 
 def roofline_for(kind, r):
     peaks = r["peaks"]
-    if kind == "decode":
+    if kind in ("decode", "tiny"):
         alg = r["gathered"] + r["idx_bytes"] + r["q_bytes"]
         achieved = alg / (r["kern_avg_ms"] * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic("decode"),
-                "algorithmic_bytes_per_launch": alg, "kernel": "sparse_mla_kernel<64> (split-K partials)",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(kind),
+                "algorithmic_bytes_per_launch": alg,
+                "kernel": "sparse_mla_kernel<%d> (split-K partials)" % (64 if kind == "decode" else 16),
                 "peak_source": peaks["source"] + " (hbm_gbs, STREAM-style copy)"}
     achieved = r["flops"] / (r["kern_avg_ms"] * 1e-3) / 1e12
     pk = peaks["bf16_tflops"]

@@ -14,6 +14,7 @@ from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsmla.so")
+CROSSOVER_TABLE = os.path.join(HERE, "crossover_gb300.json")
 
 SMLA_OK, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE, SMLA_ERR_CUDA, SMLA_ERR_DEVICE = range(6)
 KV_BF16, KV_FP8 = 0, 1
@@ -88,6 +89,10 @@ def load(path: Optional[str] = None):
         raise RuntimeError("libsmla ABI mismatch: struct sizes differ from this binding")
     if path is None:
         _lib = lib
+        # the decode/prefill crossover measured on this GPU model by sparse_top_mla_gb300.calibrate
+        # (smla_forward falls back to the library's analytical default without it)
+        if os.path.exists(CROSSOVER_TABLE):
+            lib.smla_load_crossover(CROSSOVER_TABLE.encode())
     return lib
 
 

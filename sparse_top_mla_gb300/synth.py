@@ -354,7 +354,8 @@ def config(n: int, T: Optional[int] = None, seed: Optional[int] = None) -> Workl
 
 
 class SweepPool:
-    """Config 5: one 16384-token FP8 paged context shared by every sweep point.
+    """Config 5: one 16384-token paged context (64 sequences; FP8 by default, bf16 with
+    fmt=FMT_BF16) shared by every sweep point.
 
     Each point draws its own queries and index sets (random distinct positions over
     the context, 5% set to -1). `rotations` independent index sets per point let a
@@ -362,12 +363,13 @@ class SweepPool:
     its rows from HBM rather than L2.
     """
 
-    def __init__(self, ctx: int = 16384, num_seqs: int = 64, seed: int = 1005):
+    def __init__(self, ctx: int = 16384, num_seqs: int = 64, seed: int = 1005, fmt: int = FMT_FP8):
         self.ctx = ctx
         self.num_seqs = num_seqs
+        self.fmt = fmt
         rng = np.random.default_rng(seed)
         pps = ctx // PAGE
-        self.cache, self.row_stride, self.page_stride = make_cache(rng, num_seqs * pps, FMT_FP8)
+        self.cache, self.row_stride, self.page_stride = make_cache(rng, num_seqs * pps, fmt)
         self.num_pages = num_seqs * pps
         self.block_table = shuffled_block_table(rng, num_seqs, pps)
         self.seq_lens = np.full(num_seqs, ctx, dtype=np.int32)
@@ -379,7 +381,7 @@ class SweepPool:
         idx = mask_random(rng, distinct_indices(rng, np.full(T, self.ctx - 1), topk), 0.05)
         snk = normal_f32(rng, (H,)) if sink else None
         token_seq = (np.arange(T) % self.num_seqs).astype(np.int32)
-        main = _kvset(self.cache, FMT_FP8, self.row_stride, self.page_stride, self.num_pages,
+        main = _kvset(self.cache, self.fmt, self.row_stride, self.page_stride, self.num_pages,
                       self.block_table, self.seq_lens, idx, topk)
         return Workload(f"sweep H={H} topk={topk} T={T} sink={int(sink)}", T, H, q, token_seq, main,
                         None, snk, 1.0 / math.sqrt(D_QK),

@@ -133,6 +133,8 @@ def test_crossover_table(lib, tmp_path):
     with pytest.raises(binding.SmlaError):
         binding.set_crossover([(0, 512, 0, 5)])
     binding.set_crossover([])
+    if os.path.exists(binding.CROSSOVER_TABLE):  # put the packaged calibration back
+        assert binding.load_crossover(binding.CROSSOVER_TABLE) == binding.SMLA_OK
 
 
 def test_timing_hook_pairs(lib):

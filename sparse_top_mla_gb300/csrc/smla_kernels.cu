@@ -499,12 +499,12 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
   auto cache_of = [&](const Cursor& c) { return SET_FIELD(a, set_of(a, c.tile), cache); };
   // Whole rows of tile jt into L2, one bulk prefetch per row, two tiles ahead of their loads:
   // the loads then hit L2, and DRAM serves each gathered row as one contiguous read instead of
-  // one access per 128-byte block pair. Tiles 1 and 2 are not prefetched: at kernel start every
-  // CTA's first loads already saturate DRAM.
+  // one access per 128-byte block pair. Called for tiles 3 on: at kernel start every CTA's first
+  // loads already saturate DRAM.
   auto prefetch_rows = [&](int jt, const Cursor& c) -> bool {
     int64_t off[kLdRows];
     if (!get_off(jt, c, off)) return false;
-    if (lane8 == 0 && jt >= 3) {
+    if (lane8 == 0) {
       const uint8_t* cache = cache_of(c);
       const uint32_t bytes = fmt_of(c) == 1 ? kRowFp8 : kRowBf16;
 #pragma unroll
@@ -533,23 +533,21 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       ld_issue_bf16<1>(cache, off_cur, lane8, 1, D);
     }
   }
-  // the prefetch of tile 1 goes out after tile 0's own loads
-  if (n > 1) {
-    Cursor c1 = cur;
-    c1.next(a);
-    if (!prefetch_rows(1, c1)) return;
-  }
 
   for (int j = 0; j < n; ++j) {
     const bool first = cur.tile == 0 || j == 0;
     const bool has1 = j + 1 < n;
     Cursor nxt = cur;
     nxt.next(a);
-    if (has1) {
+    auto next_rows = [&]() -> bool {
       if (nxt.tile == 0) prefetch_q(nxt.item);
-      if (!get_off(j + 1, nxt, off_nxt)) return;
-    }
-    if (j + 2 < n) {
+      return get_off(j + 1, nxt, off_nxt);
+    };
+    // rows of the next two tiles, while the tensor core still works on the previous tile; on the
+    // first tile the next rows are taken after its first store instead (at the start of the stream
+    // tile 1 is still being resolved while tile 0 is stored), and tiles 1 and 2 are not prefetched
+    if (j > 0 && has1 && !next_rows()) return;
+    if (j > 0 && j + 2 < n) {
       Cursor c2 = nxt;
       c2.next(a);
       if (!prefetch_rows(j + 2, c2)) return;
@@ -581,6 +579,9 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
         __syncwarp();
         if (lane == 0) mbar_arrive(sh.bar(bp == 1 ? kBarFullA : kBarFullB));
       }
+      // first tile: an fp8 tile's first refill already needs the next rows; a bf16 tile's
+      // first refills still read the current tile
+      if (j == 0 && bp == 0 && has1 && fmt_cur == 1 && !next_rows()) return false;
       // ---- refill the slots this store freed
       if (fmt_cur == 1) {
         if (has1) {
@@ -607,6 +608,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
           if (bp == 3) ld_issue_rope(1, cache_nxt, off_nxt, lane8, D);
         }
       }
+      if (j == 0 && bp == 0 && has1 && fmt_cur != 1 && !next_rows()) return false;
       if (fmt_cur == 1 && bp < 3) ld_dequant_fp8<(bp < 3 ? bp + 1 : 3)>(D, dq);
       return true;
     };

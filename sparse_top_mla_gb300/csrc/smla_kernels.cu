@@ -301,19 +301,28 @@ __device__ __forceinline__ void warp_col_reduce_store(float* v, int lane, float*
   }
 }
 
+// One e4m3 pair -> bf16x2: exact conversion to f16x2 and then to two fp32 values, one packed
+// fp32x2 multiply by {scale, scale} (round to nearest), one rounding to bf16 (RNE).
+__device__ __forceinline__ uint32_t dequant_pair(uint16_t pair, uint64_t scale2) {
+  uint32_t out;
+  asm("{\n .reg .b16 lo, hi;\n .reg .b32 h2;\n .reg .f32 a, b;\n .reg .b64 f, r;\n"
+      " cvt.rn.f16x2.e4m3x2 h2, %1;\n mov.b32 {lo, hi}, h2;\n"
+      " cvt.f32.f16 a, lo;\n cvt.f32.f16 b, hi;\n mov.b64 f, {a, b};\n"
+      " mul.rn.f32x2 r, f, %2;\n mov.b64 {a, b}, r;\n cvt.rn.bf16x2.f32 %0, b, a;\n}\n"
+      : "=r"(out)
+      : "h"(pair), "l"(scale2));
+  return out;
+}
+
 __device__ __forceinline__ void dequant16(const uint4 raw, float scale, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint64_t scale2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(scale2) : "f"(scale));
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu);
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
-    }
+    o[2 * i] = dequant_pair(static_cast<uint16_t>(w[i] & 0xFFFFu), scale2);
+    o[2 * i + 1] = dequant_pair(static_cast<uint16_t>(w[i] >> 16), scale2);
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);

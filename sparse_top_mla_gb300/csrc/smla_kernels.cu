@@ -832,7 +832,8 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
   const uint32_t pt = sh.tile + 8 * kBlockBytes;
   uint32_t smph = 0;
-  int nfix = 0;
+  int nfix = 0;  // rescale passes so far (phase of PFixed)
+  int ndec = 0;  // fast-pass decisions so far (phase of PReady and Decision, overflow/decision slot)
   if (n <= 0) return;
 
   // ---- index resolution, by warps 0-2 (warp 0 also takes rows 96-127, so the issuing warp
@@ -884,32 +885,32 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     const bool valid = sh.rowoff[(j & 3) * kTile + tid] >= 0;
     if (!wait_bar_w(sh, sh.bar(kBarSFull), j & 1)) return;
     tc_fence_after();
-    // the first tile of an item has no running maxima yet: it always takes the max pass
+    // the first tile of an item has no running maxima yet: it always takes the max pass, which
+    // every warp knows, so it skips the fast pass and the decision hand-shake
+    bool fix = true;
     if (!first) {
       const bool over = p_pass<NH>(a, sh, tl + TC::kS, pt, valid, tid);
-      if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[j & 1] = 1;
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sh.bar(kBarPReady));
-
-    // ---- decision: the issuing thread reads the overflow flag once all four warps arrived (the
-    // first tile of an item always takes the max pass)
-    bool fix;
-    if (warp == kIssueWarp) {
-      if (!wait_bar_w(sh, sh.bar(kBarPReady), j & 1)) return;
-      int f = 0;
-      if (lane == 0) {
-        f = first ? 1 : sh.overflow[j & 1];
-        sh.overflow[j & 1] = 0;
-        sh.decision[j & 1] = f;
-        mbar_arrive(sh.bar(kBarDecision));
+      if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[ndec & 1] = 1;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sh.bar(kBarPReady));
+      // ---- decision: the issuing thread reads the overflow flag once all four warps arrived
+      if (warp == kIssueWarp) {
+        if (!wait_bar_w(sh, sh.bar(kBarPReady), ndec & 1)) return;
+        int f = 0;
+        if (lane == 0) {
+          f = sh.overflow[ndec & 1];
+          sh.overflow[ndec & 1] = 0;
+          sh.decision[ndec & 1] = f;
+          mbar_arrive(sh.bar(kBarDecision));
+        }
+        fix = __shfl_sync(0xffffffffu, f, 0) != 0;
+      } else {
+        if (!wait_bar_w(sh, sh.bar(kBarDecision), ndec & 1)) return;
+        fix = sh.decision[ndec & 1] != 0;
       }
-      fix = __shfl_sync(0xffffffffu, f, 0) != 0;
-    } else {
-      if (!wait_bar_w(sh, sh.bar(kBarDecision), j & 1)) return;
-      fix = sh.decision[j & 1] != 0;
+      ++ndec;
     }
     if (fix) {
       if (!max_pass<NH>(a, sh, tl, pt, valid, first, smph, tid)) return;

@@ -998,8 +998,9 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       }
     } else {
       // final O: thread tid holds channel 128b + tid of every head. Within each group of 8 lanes
-      // an 8x8 butterfly transpose (3 shuffle stages) gives every lane 8 consecutive channels of
-      // one head, stored as one 16-byte write (rows 16-byte aligned, strides multiples of 8).
+      // an 8x8 transpose of the bf16 values (three exchange stages on pairs packed two to a
+      // word) gives every lane 8 consecutive channels of one head, stored as one 16-byte write
+      // (rows 16-byte aligned, strides multiples of 8).
       uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
       const int64_t hstride = a.out_stride_h;
       const int k8 = lane & 7;
@@ -1015,35 +1016,55 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
           for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
 #pragma unroll
           for (int q = 0; q < CW / 8; ++q) {
-            float* x = o + 8 * q;  // heads c0+8q .. c0+8q+7 of this lane's channel
+            // heads c0+8q .. c0+8q+7 of this lane's channel, as bf16 pairs (p[m] = heads 2m, 2m+1)
+            uint32_t p[4];
 #pragma unroll
-            for (int d = 4; d >= 1; d >>= 1) {
-              const bool upper = (k8 & d) != 0;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if ((i & d) == 0) {
-                  const float send = upper ? x[i] : x[i + d];
-                  const float recv = __shfl_xor_sync(0xffffffffu, send, d);
-                  if (upper) {
-                    x[i] = recv;
-                  } else {
-                    x[i + d] = recv;
-                  }
-                }
+            for (int m = 0; m < 4; ++m) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * q + 2 * m], o[8 * q + 2 * m + 1]);
+              p[m] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            // 8x8 transpose of bf16 elements across the 8 lanes of the group, in three exchange
+            // stages: lane pairs k, k^4 swap whole words 2,3 <-> 0,1; k, k^2 swap words 1,3 <->
+            // 0,2; k, k^1 swap the odd <-> even halves of every word (packed two to a word)
+            {
+              const bool up = (k8 & 4) != 0;
+              const uint32_t r0 = __shfl_xor_sync(0xffffffffu, up ? p[0] : p[2], 4);
+              const uint32_t r1 = __shfl_xor_sync(0xffffffffu, up ? p[1] : p[3], 4);
+              if (up) {
+                p[0] = r0;
+                p[1] = r1;
+              } else {
+                p[2] = r0;
+                p[3] = r1;
               }
+            }
+            {
+              const bool up = (k8 & 2) != 0;
+              const uint32_t r0 = __shfl_xor_sync(0xffffffffu, up ? p[0] : p[1], 2);
+              const uint32_t r1 = __shfl_xor_sync(0xffffffffu, up ? p[2] : p[3], 2);
+              if (up) {
+                p[0] = r0;
+                p[2] = r1;
+              } else {
+                p[1] = r0;
+                p[3] = r1;
+              }
+            }
+            {
+              const bool up = (k8 & 1) != 0;
+              const uint32_t sel = up ? 0x5410u : 0x7632u;  // the halves this lane gives away
+              const uint32_t q0 = __shfl_xor_sync(0xffffffffu, __byte_perm(p[0], p[1], sel), 1);
+              const uint32_t q1 = __shfl_xor_sync(0xffffffffu, __byte_perm(p[2], p[3], sel), 1);
+              const uint32_t s_lo = up ? 0x3254u : 0x5410u, s_hi = up ? 0x3276u : 0x7610u;
+              p[0] = __byte_perm(p[0], q0, s_lo);
+              p[1] = __byte_perm(p[1], q0, s_hi);
+              p[2] = __byte_perm(p[2], q1, s_lo);
+              p[3] = __byte_perm(p[3], q1, s_hi);
             }
             // lane 8g+k now holds head c0+8q+k for channels 32w+8g .. 32w+8g+7
             const int h = c0 + 8 * q + k8;
-            if (h < hg) {
-              uint32_t w4[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 bb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-                w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
-              }
-              *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) =
-                  make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            if (h < hg)
+              *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) = make_uint4(p[0], p[1], p[2], p[3]);
           }
         }
       }

@@ -1,0 +1,63 @@
+"""bench.py's JSON line and roofline arithmetic, on a fake timing result (no GPU)."""
+import json
+import os
+import sys
+import types
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from sparse_top_mla_gb300 import synth  # noqa: E402
+
+REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "roofline", "clocks", "e2e", "gpu_launches")
+
+
+def _fake(kind, w):
+    return {"label": "fake " + kind, "w0": w, "value": 1000.0, "total_ms": 7.5, "steps": 100, "l2_flush": False,
+            "ms_per_step": 0.075, "kern_avg_ms": 0.0675, "kern_samples": 25, "gathered": w.gathered_bytes(),
+            "flops": w.flops(), "idx_bytes": 524288, "q_bytes": w.T * w.H * 576 * 2,
+            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3},
+            "e2e": {"value": 500.0, "unit": "GB/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 1},
+            "launches": 200, "peaks": {"hbm_gbs": 6680.5, "bf16_tflops": 1943.9, "source": "of measured"}}
+
+
+def test_decode_line_has_the_contract_keys():
+    w = synth.config(1)
+    r = _fake("decode", w)
+    args = types.SimpleNamespace(warmup=5)
+    d = bench.line_for("decode", r, args, 1, {"value": 0.2, "unit": "GB/s", "cores": 16, "kind": "oracle",
+                                              "sample": "x"})
+    for k in REQUIRED:
+        assert k in d, k
+    json.dumps(d)
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["n_gpus"] == 1
+    rl = d["roofline"]
+    alg = r["gathered"] + r["idx_bytes"] + r["q_bytes"]
+    assert rl["bound"] == "hbm" and rl["unit"] == "GB/s"
+    assert abs(rl["achieved"] - alg / 0.0675e-3 / 1e9) < 1e-6
+    assert abs(rl["frac"] - rl["achieved"] / 6680.5) < 1e-12
+    assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_prefill_roofline_is_tensor_flops():
+    w = synth.config(1)
+    r = _fake("prefill", w)
+    rl = bench.roofline_for("prefill", r)
+    assert rl["bound"] == "tensor" and rl["unit"] == "TFLOP/s"
+    assert abs(rl["achieved"] - w.flops() / 0.0675e-3 / 1e12) < 1e-9
+    assert abs(rl["frac"] - rl["achieved"] / 1943.9) < 1e-12
+
+
+def test_traffic_only_for_the_captured_source(monkeypatch):
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: d["decode"]["kernel_source_hash"])
+    assert bench.ncu_traffic("decode") == d["decode"]["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.ncu_traffic("decode") is None
+
+
+def test_l2_rule_is_stated():
+    assert bench.input_mb(synth.config(1)) < bench.L2_MB
+    assert bench.l2_note(synth.config(1), True).startswith("L2 flushed")
+    assert "larger than L2" in bench.l2_note(synth.config(1), False)

@@ -1,7 +1,7 @@
 """Benchmark: sparse top-k MLA decode on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smla|reference]
-                    [--workload decode|prefill|large_prefill] [--extra-lines]
+                    [--workload decode|prefill|large_prefill|tiny] [--extra-lines]
 
 A step is one smla_forward call (index resolve, gather + FP8 dequant, QK^T, softmax with
 sink, PV, split-K partials, combine) over the decode workload: 64 sequences x 16384 cached
@@ -33,18 +33,25 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-MLA prefill TFLOP/s & decode µs/call + GB/s, as % of roofline"
 ROTATIONS = 8
+# about half a second of timed GPU work per workload
+DEFAULT_STEPS = {"decode": 6000, "prefill": 800, "large_prefill": 40, "tiny": 8000}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: the workload's, about half a second of GPU time, so the "
+                         "20 ms clock samples fall inside the timed region)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny"])
     ap.add_argument("--extra-lines", action="store_true",
                     help="also print one JSON line per secondary workload to stderr")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps <= 0:
+        args.steps = 50 if args.impl == "reference" else DEFAULT_STEPS[args.workload]
+    return args
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -103,21 +110,23 @@ def build_workloads(kind):
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while the timed region runs."""
+    """nvidia-smi clocks/throttle reasons sampled every 20 ms; only the samples taken while the
+    timed region ran (host wall-clock window) are summarised."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except FileNotFoundError:
@@ -125,20 +134,30 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarise(self.lines, t0, t1)
+
+    @classmethod
+    def summarise(cls, lines, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen in [t0, t1]; with no sample inside the
+        window, the samples nearest to it (and "samples_in_region": 0)."""
+        inside = [ln for t, ln in lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
+        use = inside
+        if not inside and lines and t0 is not None:
+            mid = (t0 + (t1 if t1 is not None else t0)) / 2
+            use = [min(lines, key=lambda x: abs(x[0] - mid))[1]]
         sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in use:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -147,11 +166,11 @@ class ClockSampler:
                 smax = float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(cls.REASONS, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_region": len(inside)}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -263,7 +282,7 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)
     barrier(world)
     torch.cuda.synchronize()
     # inputs that fit in L2 are evicted before every timed step by a write larger than L2; each
@@ -274,6 +293,7 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
         if flush else []
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     t_start.record(stream)
     for s in range(steps):
         p = probs[s % len(probs)]
@@ -290,9 +310,10 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
             sev[s][1].record(stream)
     t_stop.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
     barrier(world)
     binding.set_timing_events(None, None)
-    clk = clocks.stop()
+    clk = clocks.stop(wall0, wall1)
     assert binding.device_error() == 0
     elapsed = sum(a.elapsed_time(b) for a, b in sev) if flush else t_start.elapsed_time(t_stop)
     total_ms = max_over_ranks(elapsed, world)

@@ -61,3 +61,20 @@ def test_l2_rule_is_stated():
     assert bench.input_mb(synth.config(1)) < bench.L2_MB
     assert bench.l2_note(synth.config(1), True).startswith("L2 flushed")
     assert "larger than L2" in bench.l2_note(synth.config(1), False)
+
+
+def test_clock_summary_uses_the_timed_window():
+    row = "0, {sm}, 2070, 900, 0x0, Not Active, Not Active, Not Active, {cap}"
+    lines = [(10.0, row.format(sm=1200, cap="Not Active")), (10.4, row.format(sm=2070, cap="Active")),
+             (10.5, row.format(sm=2040, cap="Not Active")), (11.0, row.format(sm=1100, cap="Not Active"))]
+    c = bench.ClockSampler.summarise(lines, 10.3, 10.6)
+    assert c["samples_in_region"] == 2 and c["sm_mhz"] == 2055.0 and c["reasons"] == ["sw_power_cap"]
+    c = bench.ClockSampler.summarise(lines, 10.6, 10.7)  # nothing inside: the nearest sample
+    assert c["samples_in_region"] == 0 and c["samples"] == 1 and c["sm_mhz"] == 2040.0
+
+
+def test_default_steps_give_a_long_enough_timed_region(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    assert bench.parse().steps == bench.DEFAULT_STEPS["decode"]
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "7"])
+    assert bench.parse().steps == 7

@@ -63,6 +63,9 @@ def _load():
         lib.oracle_e4m3_value.restype = ctypes.c_double
         lib.oracle_bf16_value.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_value.restype = ctypes.c_double
+        lib.oracle_pack_rows.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_void_p]
+        lib.oracle_pack_rows.restype = ctypes.c_int
         lib.oracle_threads.argtypes = [ctypes.c_int32]
         lib.oracle_threads.restype = ctypes.c_int32
         _lib = lib
@@ -115,6 +118,20 @@ def attention(w, tokens=None, nthreads: int = 0):
     if rc != 0:
         raise ValueError("oracle rejected the problem")
     return O, lse
+
+
+def pack_rows(x, fmt: int):
+    """Cache writer: rows of 576 values (float32 array, or uint16 bf16 bits) -> row bytes
+    [n, 1152] (fmt 0, bf16) or [n, 656] (fmt 1, FP8 with per-128-channel scales)."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    assert x.ndim == 2 and x.shape[1] == 576 and x.dtype in (np.float32, np.uint16)
+    dtype = 1 if x.dtype == np.float32 else 0
+    rb = 1152 if fmt == 0 else 656
+    out = np.zeros((x.shape[0], rb), dtype=np.uint8)
+    if lib.oracle_pack_rows(_ptr(x), dtype, 576, x.shape[0], fmt, _ptr(out)) != 0:
+        raise ValueError("oracle rejected the rows")
+    return out
 
 
 def e4m3_value(code: int) -> float:

@@ -126,6 +126,82 @@ void one_token(const oracle_problem& p, int t, double* O, double* lse) {
   }
 }
 
+// ------------------------------------------------------------------ cache writer
+// Packing new latent rows into the cache (the step the pages' benchmark runs before every
+// measurement: flashinfer PR "add topk=256 prefill-dsv4 dispatch", conversation, the GB10
+// benchmark's "Method" paragraph, where both sides' KV is packed by the same quantiser).
+// The pages print no arithmetic for it; the reading taken here, per 128-channel latent block:
+//   amax  = max |x_c|                            (exact)
+//   scale = amax / 448 rounded to fp32            (1.0 when amax = 0); stored as fp32
+//   y_c   = x_c / scale rounded to fp32           (the precision of the stored scale)
+//   code  = the E4M3FN value nearest to y_c, ties to the even code, |y_c| > 448 -> 448
+// and the 64 rope channels are rounded to bf16 (nearest, ties to even).
+
+// bf16 bit pattern nearest to the fp32 value f (ties to the even pattern). The two
+// candidates are the bf16 values that bracket f; the comparison is exact in fp64.
+uint16_t bf16_nearest(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if (std::isnan(f)) return static_cast<uint16_t>((u >> 16) | 0x40);
+  const uint32_t lo = u & 0xFFFF0000u;  // truncation toward zero
+  const uint32_t hi = lo + 0x10000u;    // next bf16 away from zero
+  float flo, fhi;
+  std::memcpy(&flo, &lo, 4);
+  std::memcpy(&fhi, &hi, 4);
+  const double d_lo = std::fabs(static_cast<double>(f) - static_cast<double>(flo));
+  const double d_hi = std::isinf(fhi) ? std::numeric_limits<double>::infinity()
+                                      : std::fabs(static_cast<double>(fhi) - static_cast<double>(f));
+  uint32_t pick;
+  if (d_lo < d_hi) {
+    pick = lo;
+  } else if (d_hi < d_lo) {
+    pick = hi;
+  } else {
+    pick = ((lo >> 16) & 1u) == 0 ? lo : hi;
+  }
+  // between the largest finite bf16 and 2^128 the halfway point decides overflow to infinity
+  return static_cast<uint16_t>(pick >> 16);
+}
+
+// E4M3FN code nearest to y (saturating): searched over the 127 finite non-negative codes.
+uint8_t e4m3_nearest(float y) {
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  const double v = std::fabs(static_cast<double>(y));
+  if (v >= 448.0) return sign | 0x7E;
+  int c = 0;  // largest code whose value is <= v
+  while (c + 1 <= 0x7E && e4m3_value(static_cast<uint8_t>(c + 1)) <= v) ++c;
+  if (e4m3_value(static_cast<uint8_t>(c)) == v) return sign | static_cast<uint8_t>(c);
+  const double d_lo = v - e4m3_value(static_cast<uint8_t>(c));
+  const double d_hi = e4m3_value(static_cast<uint8_t>(c + 1)) - v;
+  int pick = d_lo < d_hi ? c : (d_hi < d_lo ? c + 1 : ((c & 1) == 0 ? c : c + 1));
+  return sign | static_cast<uint8_t>(pick);
+}
+
+// One row of 576 fp32 values -> row bytes of format fmt.
+void pack_row(const float* x, int32_t fmt, uint8_t* out) {
+  if (fmt == 0) {
+    for (int c = 0; c < kDqk; ++c) {
+      const uint16_t b = bf16_nearest(x[c]);
+      std::memcpy(out + 2 * c, &b, 2);
+    }
+    return;
+  }
+  for (int blk = 0; blk < 4; ++blk) {
+    float amax = 0.0f;
+    for (int c = 128 * blk; c < 128 * (blk + 1); ++c) amax = std::max(amax, std::fabs(x[c]));
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int c = 128 * blk; c < 128 * (blk + 1); ++c) {
+      const float y = x[c] / scale;
+      out[c] = e4m3_nearest(y);
+    }
+    std::memcpy(out + kDv + 4 * blk, &scale, 4);
+  }
+  for (int c = 0; c < kDqk - kDv; ++c) {
+    const uint16_t b = bf16_nearest(x[kDv + c]);
+    std::memcpy(out + kDv + 16 + 2 * c, &b, 2);
+  }
+}
+
 bool malformed(const oracle_kvset& s) {
   return s.cache == nullptr || s.block_table == nullptr || s.seq_lens == nullptr ||
          s.indices == nullptr || s.topk < 0 || s.idx_stride < s.topk || (s.fmt != 0 && s.fmt != 1);
@@ -142,6 +218,27 @@ int32_t oracle_threads(int32_t requested) {
   if (requested > 0) return requested;
   const unsigned hw = std::thread::hardware_concurrency();
   return hw ? static_cast<int32_t>(hw) : 1;
+}
+
+int oracle_pack_rows(const void* x, int32_t x_dtype, int64_t x_stride, int32_t n, int32_t fmt, uint8_t* out) {
+  if (n < 0 || (n > 0 && (!x || !out)) || (fmt != 0 && fmt != 1) || (x_dtype != 0 && x_dtype != 1) ||
+      x_stride < kDqk)
+    return -1;
+  const int row_bytes = fmt == 0 ? 2 * kDqk : kDv + 16 + 2 * (kDqk - kDv);
+  std::vector<float> row(kDqk);
+  for (int32_t i = 0; i < n; ++i) {
+    for (int c = 0; c < kDqk; ++c) {
+      if (x_dtype == 0) {
+        uint16_t b;
+        std::memcpy(&b, static_cast<const uint8_t*>(x) + 2 * (static_cast<int64_t>(i) * x_stride + c), 2);
+        row[c] = static_cast<float>(bf16_value(b));
+      } else {
+        std::memcpy(&row[c], static_cast<const uint8_t*>(x) + 4 * (static_cast<int64_t>(i) * x_stride + c), 4);
+      }
+    }
+    pack_row(row.data(), fmt, out + static_cast<int64_t>(i) * row_bytes);
+  }
+  return 0;
 }
 
 int oracle_attention(const oracle_problem* p, const int32_t* tokens, int32_t n, double* O,

@@ -70,6 +70,14 @@ typedef struct {
 int oracle_attention(const oracle_problem* p, const int32_t* tokens, int32_t n, double* O,
                      double* lse, int32_t nthreads);
 
+/* Cache writer: packs n rows of 576 values (x_dtype 0 = bf16 bits, 1 = fp32; row i at
+ * element offset i*x_stride) into row bytes of format fmt (0 bf16: 1152 B, 1 fp8: 656 B),
+ * written contiguously to out [n, row_bytes]. fp8 reading: per 128 latent channels
+ * scale = fl32(amax/448) (1 if amax = 0), code = nearest E4M3FN to fl32(x/scale), ties to
+ * even, saturating at 448; rope and bf16 rows: nearest bf16, ties to even.
+ * Returns 0, or -1 on malformed arguments. */
+int oracle_pack_rows(const void* x, int32_t x_dtype, int64_t x_stride, int32_t n, int32_t fmt, uint8_t* out);
+
 /* Exact value of one OCP E4M3FN code (NaN for S.1111.111). */
 double oracle_e4m3_value(uint8_t code);
 /* Exact value of one bfloat16 bit pattern. */

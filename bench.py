@@ -1,18 +1,23 @@
-"""Benchmark: sparse top-k MLA decode on one GB300 (or N independent replicas).
+"""Benchmark: sparse top-k MLA attention on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smla|reference]
-                    [--workload decode|prefill|large_prefill|tiny] [--extra-lines]
+                    [--workload decode|prefill|large_prefill|tiny] [--no-secondary]
 
-A step is one smla_forward call (index resolve, gather + FP8 dequant, QK^T, softmax with
-sink, PV, split-K partials, combine) over the decode workload: 64 sequences x 16384 cached
-tokens, T = 64 query tokens, H = 64 heads, top-k 2048 (5% masked), FP8 KV, per-head sink.
-Eight index sets (and query sets) rotate between steps so that every call gathers its rows
-from HBM (8 x 81.7 MB of distinct rows > the 129 MB L2); the cache itself is 688 MB.
+The headline step is one smla_forward call (index resolve, gather + FP8 dequant, QK^T,
+softmax with sink, PV, split-K partials, combine) over the decode workload: 64 sequences x
+16384 cached tokens, T = 64 query tokens, H = 64 heads, top-k 2048 (5% masked), FP8 KV,
+per-head sink. Eight index sets (and query sets) rotate between steps so that every call
+gathers its rows from HBM (8 x 81.7 MB of distinct rows > the 129 MB L2); the cache itself is
+688 MB.
 
 One JSON line is printed by rank 0. `value` is gathered-KV GB/s over all ranks; `e2e`
 repeats the measurement with the step's inputs copied from pinned host memory and the
-outputs copied back inside the timed region. `--impl reference` times the fp64 CPU oracle
-(the only other implementation this project has) on the same workload and metric.
+outputs copied back inside the timed region. With the default decode workload the same line
+also carries the prefill (T=4096, H=32, topk=512, bf16) and large-prefill (T=8192, H=128,
+topk=2048+128, FP8 + bf16 extra cache) workloads under config.prefill and
+config.large_prefill, each timed for K steps with its own TFLOP/s roofline and an oracle
+CPU baseline on a token sample. `--impl reference` times the fp64 CPU oracle (the only
+other implementation this project has) on the same workload and metric.
 """
 from __future__ import annotations
 
@@ -46,9 +51,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny"])
-    ap.add_argument("--extra-lines", action="store_true",
-                    help="also print one JSON line per secondary workload to stderr")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="decode only: leave the prefill and large-prefill workloads out of the line")
     args = ap.parse_args()
+    args.steps_given = args.steps > 0
     if args.steps <= 0:
         args.steps = 50 if args.impl == "reference" else DEFAULT_STEPS[args.workload]
     return args
@@ -117,6 +123,16 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
+    @classmethod
+    def once(cls, gpu_index):
+        """One read-only sample (host time, csv line), or None without nvidia-smi."""
+        try:
+            r = subprocess.run(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={cls.FIELDS}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            return (time.time(), r.stdout.strip()) if r.returncode == 0 else None
+        except (FileNotFoundError, subprocess.TimeoutExpired):
+            return None
+
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
@@ -136,7 +152,7 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self, t0=None, t1=None):
+    def stop(self, t0=None, t1=None, bracket=()):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.05)
@@ -145,15 +161,18 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        return self.summarise(self.lines, t0, t1)
+        return self.summarise(self.lines, t0, t1, bracket)
 
     @classmethod
-    def summarise(cls, lines, t0=None, t1=None):
-        """Median SM clock and the throttle reasons seen in [t0, t1]; with no sample inside the
-        window, the samples nearest to it (and "samples_in_region": 0)."""
+    def summarise(cls, lines, t0=None, t1=None, bracket=()):
+        """Median SM clock and the throttle reasons seen in [t0, t1]. `bracket` holds the one-shot
+        samples taken just before the timed region started and just after it ended; they are
+        always summarised with the samples inside the window, so a region shorter than the
+        20 ms sampling period still has a clock record next to it."""
         inside = [ln for t, ln in lines if (t0 is None or t >= t0) and (t1 is None or t <= t1)]
-        use = inside
-        if not inside and lines and t0 is not None:
+        edge = [b[1] for b in bracket if b is not None]
+        use = inside + edge
+        if not use and lines and t0 is not None:
             mid = (t0 + (t1 if t1 is not None else t0)) / 2
             use = [min(lines, key=lambda x: abs(x[0] - mid))[1]]
         sm, smax, reasons = [], None, set()
@@ -170,7 +189,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm), "samples_in_region": len(inside)}
+                "samples": len(sm), "samples_in_region": len(inside), "bracket_samples": len(edge)}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -246,7 +265,7 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- smla arm
-def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
+def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True):
     import torch
     from sparse_top_mla_gb300 import binding
     dev = torch.device(f"cuda:{local}")
@@ -293,6 +312,7 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
         if flush else []
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
+    before = ClockSampler.once(local)
     wall0 = time.time()
     t_start.record(stream)
     for s in range(steps):
@@ -311,9 +331,10 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
     t_stop.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
+    after = ClockSampler.once(local)
     barrier(world)
     binding.set_timing_events(None, None)
-    clk = clocks.stop(wall0, wall1)
+    clk = clocks.stop(wall0, wall1, (before, after))
     assert binding.device_error() == 0
     elapsed = sum(a.elapsed_time(b) for a, b in sev) if flush else t_start.elapsed_time(t_stop)
     total_ms = max_over_ranks(elapsed, world)
@@ -325,6 +346,16 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
     decode_route = w0.T <= binding.decode_max_tokens(w0.H, w0.main.topk + (w0.extra.topk if w0.extra else 0),
                                                       w0.main.fmt)
     launches_per_step = 2 if (decode_route and splits_used) else 1
+
+    peaks = measured_peaks()
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    res = {"label": label, "w0": w0, "value": value, "total_ms": total_ms, "steps": steps, "l2_flush": flush,
+           "ms_per_step": total_ms / steps, "kern_avg_ms": kern_avg_ms, "kern_samples": len(kern_ms),
+           "gathered": gathered[0], "flops": flops, "idx_bytes": idx_bytes, "q_bytes": q_bytes,
+           "alg_bytes": w0.algorithmic_bytes(), "clocks": clk, "launches": launches_per_step * steps,
+           "peaks": peaks}
+    if not with_e2e:
+        return res
 
     # e2e: pinned host inputs -> device, forward, outputs -> pinned host, every step
     h_q = [torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory() for w in rots]
@@ -364,14 +395,27 @@ def time_workload(kind, steps, warmup, world, rank, local, with_cpu_baseline):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = sum(gathered[s % len(probs)] for s in range(e2e_steps)) * world / (e2e_ms * 1e-3) / 1e9
 
-    peaks = measured_peaks()
-    kern_avg_ms = sum(kern_ms) / len(kern_ms)
-    res = {"label": label, "w0": w0, "value": value, "total_ms": total_ms, "steps": steps, "l2_flush": flush,
-           "ms_per_step": total_ms / steps, "kern_avg_ms": kern_avg_ms, "kern_samples": len(kern_ms),
-           "gathered": gathered[0], "flops": flops, "idx_bytes": idx_bytes, "q_bytes": q_bytes, "clocks": clk,
-           "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                   "steps": e2e_steps}, "launches": launches_per_step * steps, "peaks": peaks}
+    res["e2e"] = {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                  "steps": e2e_steps}
     return res
+
+
+def cpu_baseline_tokens(kind, n_tok):
+    """The oracle on a seeded sample of n_tok query tokens of a prefill workload, scaled to
+    TFLOP/s (tokens are independent, so work is proportional to the tokens computed)."""
+    import oracle
+    from sparse_top_mla_gb300 import synth
+    oracle.build()
+    w = synth.config(3) if kind == "prefill" else synth.config(4)
+    tok = np.sort(np.random.default_rng(99).choice(w.T, size=n_tok, replace=False))
+    threads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.attention(w, tokens=tok, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = w.flops() * n_tok / w.T
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_tok} of {w.T} query tokens (seeded), all heads and entries, fp64 oracle",
+            "seconds": dt}
 
 
 def cpu_baseline_decode():
@@ -391,18 +435,26 @@ def cpu_baseline_decode():
 def roofline_for(kind, r):
     peaks = r["peaks"]
     if kind in ("decode", "tiny"):
-        alg = r["gathered"] + r["idx_bytes"] + r["q_bytes"]
-        achieved = alg / (r["kern_avg_ms"] * 1e-3) / 1e9
+        # algorithmic bytes of one call (valid gathered rows, indices, q, O, LSE) over the
+        # dominant kernel's time; the gathered-rows-only fraction is reported beside it
+        alg = r["alg_bytes"]
+        ks = r["kern_avg_ms"] * 1e-3
+        achieved = alg / ks / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(kind),
                 "algorithmic_bytes_per_launch": alg,
+                "frac_gathered": r["gathered"] / ks / 1e9 / peaks["hbm_gbs"],
+                "frac_call": alg / (r["ms_per_step"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "kernel": "sparse_mla_kernel<%d> (split-K partials)" % (64 if kind == "decode" else 16),
                 "peak_source": peaks["source"] + " (hbm_gbs, STREAM-style copy)"}
     achieved = r["flops"] / (r["kern_avg_ms"] * 1e-3) / 1e12
     pk = peaks["bf16_tflops"]
     return {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
             "traffic": ncu_traffic(kind), "algorithmic_flops_per_launch": r["flops"],
-            "peak_source": peaks["source"] + " (bf16_tflops burst, cuBLAS)"}
+            "frac_sustained": achieved / peaks["bf16_tflops_sustained"] if peaks.get("bf16_tflops_sustained")
+            else None,
+            "peak_source": peaks["source"] + " (bf16_tflops burst, cuBLAS; frac_sustained against the "
+                                             "sustained figure)"}
 
 
 L2_MB = 129.0
@@ -446,6 +498,20 @@ def line_for(kind, r, args, world, cpu):
     return d
 
 
+def secondary_for(kind, r, cpu):
+    """The prefill-type workload as a sub-object of the decode line (TFLOP/s headline)."""
+    us = r["ms_per_step"] * 1e3
+    d = {"workload": r["label"], "value": r["flops"] / (r["ms_per_step"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+         "us_per_call": us, "kernel_avg_us": r["kern_avg_ms"] * 1e3, "kernel_timed_steps": r["kern_samples"],
+         "steps": r["steps"], "gathered_bytes_per_call": r["gathered"],
+         "gathered_gbs": r["gathered"] / (r["ms_per_step"] * 1e-3) / 1e9,
+         "l2": l2_note(r["w0"], r["l2_flush"]), "roofline": roofline_for(kind, r), "clocks": r["clocks"],
+         "gpu_launches": r["launches"]}
+    if cpu is not None:
+        d["cpu_baseline"] = cpu
+    return d
+
+
 def main():
     args = parse()
     world, rank, local = dist_init(args.gpus)
@@ -461,13 +527,20 @@ def main():
     barrier(world)
     r = time_workload(args.workload, args.steps, args.warmup, world, rank, local, True)
     cpu = cpu_baseline_decode() if (rank == 0 and world == 1 and args.workload == "decode") else None
+    line = line_for(args.workload, r, args, world, cpu)
+    if args.workload == "decode" and not args.no_secondary:
+        # the prefill half of the metric, in the same line: each workload timed for the same
+        # number of steps when --steps is given, else for its own default (about half a second)
+        for kind, n_tok in (("prefill", 256), ("large_prefill", 16)):
+            steps = args.steps if args.steps_given else DEFAULT_STEPS[kind]
+            rr = time_workload(kind, steps, args.warmup, world, rank, local, False)
+            cpu_k = cpu_baseline_tokens(kind, n_tok) if (rank == 0 and world == 1) else None
+            line["config"][kind] = secondary_for(kind, rr, cpu_k)
+            line["gpu_launches"] += rr["launches"]
+            import torch
+            torch.cuda.empty_cache()
     if rank == 0:
-        print(json.dumps(line_for(args.workload, r, args, world, cpu)), flush=True)
-    if args.extra_lines:
-        for kind in ("prefill", "large_prefill"):
-            rr = time_workload(kind, max(3, args.steps // 5), args.warmup, world, rank, local, False)
-            if rank == 0:
-                print(json.dumps(line_for(kind, rr, args, world, None)), file=sys.stderr, flush=True)
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -144,6 +144,29 @@ smla_status smla_decode(const smla_params* p, smla_stream_t stream);
  * them. Results equal smla_decode's. */
 smla_status smla_decode_static(const smla_params* p, smla_stream_t stream);
 
+/* Cache writer: packs n new latent rows into a paged cache (the step that fills the cache
+ * this library reads; the pages' benchmark packs its KV with such a quantiser before every
+ * measurement: flashinfer PR "add topk=256 prefill-dsv4 dispatch", conversation, GB10
+ * benchmark "Method" paragraph).
+ *   kv        device [n, kv_stride] rows of 576 values (512 latent + 64 rope), bf16
+ *             (kv_dtype = SMLA_IN_BF16) or fp32 (SMLA_IN_F32); 16-byte aligned, kv_stride
+ *             in elements, kv_stride * element size a multiple of 16.
+ *   slots     device int64 [n]: physical row of each new token, page * 64 + row in page;
+ *             a slot < 0 or >= num_pages * 64 skips that row (nothing is written).
+ *   cache     device bytes laid out as smla_kv_set describes (row/page strides, num_pages).
+ *   format    SMLA_KV_BF16: every channel rounded to bf16 (nearest, ties to even; a bf16
+ *             input is copied). SMLA_KV_FP8_E4M3_S128: per 128 latent channels
+ *             scale = amax / 448 in fp32 (1 for an all-zero block), code = E4M3FN of the fp32
+ *             quotient x / scale rounded to nearest even and saturated to +-448; rope
+ *             rounded to bf16. The reading of the pages is ours: they give no arithmetic.
+ * Inputs are expected to be finite. Rows written by two entries with the same slot race.
+ * Argument errors return before any launch; enqueued on `stream` only. */
+typedef enum { SMLA_IN_BF16 = 0, SMLA_IN_F32 = 1 } smla_in_dtype;
+smla_status smla_quantize_kv(const void* kv, int32_t kv_dtype, int64_t kv_stride, int32_t n,
+                             const int64_t* slots, void* cache, int32_t format,
+                             int64_t row_stride_bytes, int64_t page_stride_bytes, int32_t num_pages,
+                             smla_stream_t stream);
+
 /* Calibrated dispatch (flashinfer PR "explain ..." merged body, Dispatch: crossover —
  * decode serves T <= decode_max_tokens for the configuration, prefill serves the rest).
  * Routes to smla_decode when T <= smla_decode_max_tokens(H, topk total, main format),

@@ -163,17 +163,23 @@ uint16_t bf16_nearest(float f) {
   return static_cast<uint16_t>(pick >> 16);
 }
 
-// E4M3FN code nearest to y (saturating): searched over the 127 finite non-negative codes.
+// E4M3FN code nearest to y (saturating): searched over the 127 finite non-negative codes,
+// whose values increase with the code.
 uint8_t e4m3_nearest(float y) {
+  static const std::vector<double> values = [] {
+    std::vector<double> v(0x7F);
+    for (int c = 0; c < 0x7F; ++c) v[c] = e4m3_value(static_cast<uint8_t>(c));
+    return v;
+  }();
   const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
   const double v = std::fabs(static_cast<double>(y));
   if (v >= 448.0) return sign | 0x7E;
-  int c = 0;  // largest code whose value is <= v
-  while (c + 1 <= 0x7E && e4m3_value(static_cast<uint8_t>(c + 1)) <= v) ++c;
-  if (e4m3_value(static_cast<uint8_t>(c)) == v) return sign | static_cast<uint8_t>(c);
-  const double d_lo = v - e4m3_value(static_cast<uint8_t>(c));
-  const double d_hi = e4m3_value(static_cast<uint8_t>(c + 1)) - v;
-  int pick = d_lo < d_hi ? c : (d_hi < d_lo ? c + 1 : ((c & 1) == 0 ? c : c + 1));
+  // c = largest code whose value is <= v
+  const int c = static_cast<int>(std::upper_bound(values.begin(), values.end(), v) - values.begin()) - 1;
+  if (values[c] == v) return sign | static_cast<uint8_t>(c);
+  const double d_lo = v - values[c];
+  const double d_hi = values[c + 1] - v;
+  const int pick = d_lo < d_hi ? c : (d_hi < d_lo ? c + 1 : ((c & 1) == 0 ? c : c + 1));
   return sign | static_cast<uint8_t>(pick);
 }
 
@@ -225,19 +231,30 @@ int oracle_pack_rows(const void* x, int32_t x_dtype, int64_t x_stride, int32_t n
       x_stride < kDqk)
     return -1;
   const int row_bytes = fmt == 0 ? 2 * kDqk : kDv + 16 + 2 * (kDqk - kDv);
-  std::vector<float> row(kDqk);
-  for (int32_t i = 0; i < n; ++i) {
-    for (int c = 0; c < kDqk; ++c) {
-      if (x_dtype == 0) {
-        uint16_t b;
-        std::memcpy(&b, static_cast<const uint8_t*>(x) + 2 * (static_cast<int64_t>(i) * x_stride + c), 2);
-        row[c] = static_cast<float>(bf16_value(b));
-      } else {
-        std::memcpy(&row[c], static_cast<const uint8_t*>(x) + 4 * (static_cast<int64_t>(i) * x_stride + c), 4);
+  // rows are independent: split them over threads
+  const int32_t nt = std::max<int32_t>(1, std::min<int32_t>(oracle_threads(0), n / 1024 + 1));
+  auto work = [&](int32_t r0, int32_t r1) {
+    std::vector<float> row(kDqk);
+    for (int32_t i = r0; i < r1; ++i) {
+      for (int c = 0; c < kDqk; ++c) {
+        if (x_dtype == 0) {
+          uint16_t b;
+          std::memcpy(&b, static_cast<const uint8_t*>(x) + 2 * (static_cast<int64_t>(i) * x_stride + c), 2);
+          row[c] = static_cast<float>(bf16_value(b));
+        } else {
+          std::memcpy(&row[c], static_cast<const uint8_t*>(x) + 4 * (static_cast<int64_t>(i) * x_stride + c), 4);
+        }
       }
+      pack_row(row.data(), fmt, out + static_cast<int64_t>(i) * row_bytes);
     }
-    pack_row(row.data(), fmt, out + static_cast<int64_t>(i) * row_bytes);
-  }
+  };
+  e4m3_nearest(0.0f);  // build the code table before the threads start
+  std::vector<std::thread> pool;
+  for (int32_t k = 1; k < nt; ++k)
+    pool.emplace_back(work, static_cast<int32_t>(static_cast<int64_t>(n) * k / nt),
+                      static_cast<int32_t>(static_cast<int64_t>(n) * (k + 1) / nt));
+  work(0, static_cast<int32_t>(static_cast<int64_t>(n) / nt));
+  for (auto& th : pool) th.join();
   return 0;
 }
 

@@ -20,7 +20,7 @@ SMLA_OK, SMLA_ERR_INVALID, SMLA_ERR_UNSUPPORTED, SMLA_ERR_WORKSPACE, SMLA_ERR_CU
 KV_BF16, KV_FP8 = 0, 1
 
 EXPORTS = ("smla_supported", "smla_workspace_size", "smla_prefill", "smla_decode", "smla_decode_static",
-           "smla_forward",
+           "smla_forward", "smla_quantize_kv",
            "smla_decode_max_tokens", "smla_set_crossover", "smla_load_crossover", "smla_status_string",
            "smla_device_error", "smla_last_error", "smla_set_timing_events", "smla_struct_size", "smla_version")
 
@@ -71,6 +71,8 @@ def load(path: Optional[str] = None):
         "smla_decode": ([P, vp], ctypes.c_int),
         "smla_decode_static": ([P, vp], ctypes.c_int),
         "smla_forward": ([P, vp], ctypes.c_int),
+        "smla_quantize_kv": ([vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, vp, vp, ctypes.c_int32,
+                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, vp], ctypes.c_int),
         "smla_decode_max_tokens": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_int32),
         "smla_set_crossover": ([ctypes.POINTER(ctypes.c_int32), ctypes.c_int32], ctypes.c_int),
         "smla_load_crossover": ([ctypes.c_char_p], ctypes.c_int),
@@ -215,6 +217,25 @@ def forward(call: Call, stream=None, check: bool = True) -> int:
     if check:
         _check(st, "smla_forward", call)
     return st
+
+
+def quantize_kv(kv, slots, cache, fmt: int, row_stride: int, page_stride: int, num_pages: int, stream=None,
+                check: bool = True) -> int:
+    """smla_quantize_kv: pack rows of kv (torch bf16 or float32 [n, 576], row stride >= 576) into
+    the device cache (uint8 tensor) at physical slots (int64 [n], page * 64 + row)."""
+    import torch
+    assert kv.dim() == 2 and kv.shape[1] == 576 and kv.stride(1) == 1
+    assert kv.dtype in (torch.bfloat16, torch.float32) and slots.dtype == torch.int64
+    dtype = 1 if kv.dtype == torch.float32 else 0
+    st = load().smla_quantize_kv(kv.data_ptr(), dtype, row_stride_of(kv), kv.shape[0], slots.data_ptr(),
+                                 cache.data_ptr(), fmt, row_stride, page_stride, num_pages, _stream(stream))
+    if check:
+        _check(st, "smla_quantize_kv")
+    return st
+
+
+def row_stride_of(t) -> int:
+    return row_stride(t, 0)
 
 
 def decode_max_tokens(H: int, topk_total: int, fmt: int) -> int:

@@ -181,8 +181,8 @@ Plan make_plan(const smla_params* p, bool split_k) {
   pl.workspace_bytes = 0;
   if (pl.split && p->T > 0) {
     const size_t n = static_cast<size_t>(pl.max_slots) * p->T * p->H;
-    const size_t hp = (static_cast<size_t>(p->H) + 7) & ~static_cast<size_t>(7);
-    pl.part_o_bytes = (static_cast<size_t>(pl.max_slots) * p->T * kDv * hp * sizeof(uint16_t) + 255) &
+    const size_t heads = static_cast<size_t>(pl.groups) * pl.heads_per_group;  // a multiple of 8
+    pl.part_o_bytes = (static_cast<size_t>(pl.max_slots) * p->T * kDv * heads * sizeof(uint16_t) + 255) &
                       ~static_cast<size_t>(255);
     pl.workspace_bytes = pl.part_o_bytes + ((n * sizeof(float) + 255) & ~static_cast<size_t>(255));
   }
@@ -255,7 +255,7 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
   a.split = pl.split;
   a.nctas = pl.nctas;
   a.max_slots = pl.max_slots;
-  a.hp = (p->H + 7) & ~7;
+  a.nchunks = pl.groups * pl.heads_per_group / 8;
   a.n_items = pl.n_items;
   a.total_tiles = pl.total_tiles;
   a.scale_log2 = p->sm_scale * 1.4426950408889634f;

@@ -42,7 +42,8 @@ struct AttnArgs {
   int64_t out_stride_t, out_stride_h;
   float* lse;
   int64_t lse_stride_t;
-  void* part_o;     // bf16 [max_slots, T, 512, hp] normalised partial O^T (split schedule only)
+  void* part_o;     // bf16 [max_slots, T, nchunks, 512, 8] normalised partial O^T in head chunks of 8
+                    // (split schedule only)
   float* part_lse;  // [max_slots, T, H] base-2 log-sum-exp of each partial
   KvSetDev set[2];
   int32_t nsets;
@@ -53,7 +54,7 @@ struct AttnArgs {
   int32_t split;           // 0: whole items per CTA, final outputs; 1: contiguous tile ranges, partials
   int32_t nctas;           // persistent CTAs (grid size)
   int32_t max_slots;       // partial slots per item (split schedule)
-  int32_t hp;              // H rounded up to a multiple of 8 (head stride of the partials)
+  int32_t nchunks;         // head chunks of 8 per token in the partials: groups * heads_per_group / 8
   int64_t n_items;         // T * groups
   int64_t total_tiles;     // n_items * tiles_per_item
   float scale_log2;        // sm_scale * log2(e)

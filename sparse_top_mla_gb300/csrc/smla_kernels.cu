@@ -46,6 +46,29 @@ namespace smla {
 
 __device__ int g_device_error;
 
+// Event timestamps (global timer, ns) per CTA for timeline analysis; compiled in only with
+// -DSMLA_TRACE. Slot layout: 0 entry, 1 after the dependency wait, 2 exit, 3 first rows
+// published, 4 first loads issued; tile j < 24 at 8 + 10j: +0 S^T ready, +1 fast pass done,
+// +2 decision known, +3 PV issued, +4 blocks 0-3 stored (issuer), +5 blocks 4-8 stored
+// (issuer), +6/+7 the loaders' arrivals, +8/+9 epilogue start/end.
+#ifdef SMLA_TRACE
+__device__ unsigned long long g_trace[1024][256];
+#define SMLA_TRACE_AT(slot)                                                  \
+  do {                                                                       \
+    unsigned long long t_;                                                   \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                  \
+    if (blockIdx.x < 1024 && (slot) < 256) g_trace[blockIdx.x][(slot)] = t_; \
+  } while (0)
+#define SMLA_TRACE_TILE(j, k) SMLA_TRACE_AT(((j) < 24 ? 8 + 10 * (j) + (k) : 255))
+#else
+#define SMLA_TRACE_AT(slot) \
+  do {                      \
+  } while (0)
+#define SMLA_TRACE_TILE(j, k) \
+  do {                        \
+  } while (0)
+#endif
+
 namespace {
 
 using namespace ptx;
@@ -542,6 +565,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
       ld_issue_bf16<1>(cache, off_cur, lane8, 1, D);
     }
   }
+  if (u == 0) SMLA_TRACE_AT(4);
 
   for (int j = 0; j < n; ++j) {
     const bool first = cur.tile == 0 || j == 0;
@@ -572,6 +596,8 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
+      if (u == 0 && j == 2 && bp == 2) SMLA_TRACE_AT(5);
+      if (u == 0 && j == 2 && bp == 3) SMLA_TRACE_AT(7);
       if (bp == 0 && first && j > 0) load_q(cur.item);
       if (fmt_cur == 1) {
         ld_store_fp8<bp>(sh, rg, lane8, bp, D, dq);
@@ -582,11 +608,13 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
 #pragma unroll
         for (int k = 0; k < kLdRows; ++k) sts_v4(sh.tile + 8 * kBlockBytes + swz(rg + 32 * k, lane8), D.rope[k]);
       }
+      if (u == 0 && j == 2 && bp == 2) SMLA_TRACE_AT(6);
       if (bp == 0 && first) cp_async_wait_all();
       if (bp & 1) {  // blocks 0-3 (after bp 1) or 4-8 (after bp 3) complete
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(sh.bar(bp == 1 ? kBarFullA : kBarFullB));
+        if (u == 0) SMLA_TRACE_TILE(j, bp == 1 ? 6 : 7);
       }
       // first tile: an fp8 tile's first refill already needs the next rows; a bf16 tile's
       // first refills still read the current tile
@@ -663,6 +691,7 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
     if (kb == 0 || kb == 4) {
       if (!wait_bar_w(sh, sh.bar(kb == 0 ? kBarFullA : kBarFullB), j & 1)) return false;
       tc_fence_after();
+      if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, kb == 0 ? 4 : 5);
     }
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
@@ -718,6 +747,7 @@ __device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem,
     if (bp == 3) mma_rowsum<NH>(d, tmem, first);
     mma_pv<NH>(sh, d, tmem, bp, first);
   }
+  if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, 3);
   if (j + 1 >= n) return true;
   if (!mma_qk<NH>(sh, d, tmem, j + 1)) return false;
   mma_commit_warp(sh.bar(kBarSFull));
@@ -832,6 +862,8 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
   const uint32_t pt = sh.tile + 8 * kBlockBytes;
   uint32_t smph = 0;
+  bool tr_first = true;  // first epilogue of the CTA (event timestamps only)
+  (void)tr_first;
   int nfix = 0;  // rescale passes so far (phase of PFixed)
   int ndec = 0;  // fast-pass decisions so far (phase of PReady and Decision, overflow/decision slot)
   if (n <= 0) return;
@@ -869,6 +901,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
 #pragma unroll 1
     for (int j = -5; j < 0; ++j) resolve_step(j);
   }
+  if (tid == 0) SMLA_TRACE_AT(3);
 
   if (warp == kIssueWarp && !mma_issue_first<NH>(sh, tmem)) return;
 
@@ -885,11 +918,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     const bool valid = sh.rowoff[(j & 3) * kTile + tid] >= 0;
     if (!wait_bar_w(sh, sh.bar(kBarSFull), j & 1)) return;
     tc_fence_after();
+    if (tid == 0) SMLA_TRACE_TILE(j, 0);
     // the first tile of an item has no running maxima yet: it always takes the max pass, which
     // every warp knows, so it skips the fast pass and the decision hand-shake
     bool fix = true;
     if (!first) {
       const bool over = p_pass<NH>(a, sh, tl + TC::kS, pt, valid, tid);
+      if (tid == 0) SMLA_TRACE_TILE(j, 1);
       if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[ndec & 1] = 1;
       fence_proxy_async_smem();
       tc_fence_before();
@@ -921,14 +956,19 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     }
     if (warp == kIssueWarp) {
       if (fix && !wait_bar_w(sh, sh.bar(kBarPFixed), nfix & 1)) return;
+      if (lane == 0) SMLA_TRACE_TILE(j, 2);
       if (!mma_issue_after<NH>(sh, tmem, j, n, first)) return;
     }
     if (fix) ++nfix;
 
     if (!last) continue;
-    // ---- epilogue of the item segment: wait for its last PV (and row sums)
+    // ---- epilogue of the item segment: wait for its last PV (and row sums). Every TMEM lane of
+    // L holds the same row sums, so each warp derives the output factors of the heads it writes
+    // from its own lanes: no step across warps (the issuing warp may still be queueing the next
+    // tile's QK^T while the other warps write). Warp 0 also writes the LSEs.
     if (!wait_bar_w(sh, sh.bar(kBarPvDone + 3), j & 1)) return;
     tc_fence_after();
+    if (tid == 0) SMLA_TRACE_TILE(j, 8);
     const uint32_t t = item_token(a, cur.item);
     const int h0 = item_head0(a, cur.item);
     const int hg = min(a.heads_per_group, a.H - h0);
@@ -936,50 +976,59 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
                                                                                  a.tiles_per_item,
                                                                              a.total_tiles, a.nctas))
                              : 0;
-    // warp w reads the row sums of heads 16w..16w+15 (every lane holds the same sums); lane
-    // i < 16 turns head 16w+i's sum into the output factor and the LSE
-    if (warp * 16 < NH) {
-      float l[16];
-      tmem_load<16>(tl + TC::kL + warp * 16, l);
-      if (lane < 16) {
-        const int h = warp * 16 + lane;
-        float lh = l[0];
+#pragma unroll 1
+    for (int c0 = 0; c0 < NH; c0 += CW) {
+      if (c0 >= hg) break;
+      // output factor 1 / (row sum + e^(sink - m)) of heads c0 .. c0+CW-1 (sink only for final
+      // outputs; the combine applies it to split partials); 0 for an empty head. Lane i works
+      // out head c0+i's factor (and warp 0 its LSE) into this warp's row of the reduction
+      // area, which the max pass does not use until every warp has left its epilogue.
+      float* fw = sh.red + warp * 64;
+      {
+        float l[CW];
+        tmem_load<CW>(tl + TC::kL + c0, l);
+        if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(248);
+        float lsel = l[0];
 #pragma unroll
-        for (int i = 1; i < 16; ++i) lh = (i == lane) ? l[i] : lh;
-        const float m = sh.m_run[h];
-        float factor = 0.f, lse2 = -INFINITY;
-        if (lh > 0.f) {
-          lse2 = m + log2f(lh);
-          float denom = lh;
+        for (int i = 1; i < CW; ++i) lsel = (i == lane) ? l[i] : lsel;
+        if (lane < CW) {
+          const int h = c0 + lane;
+          const float m = sh.m_run[h];
+          float denom = lsel;
           if (!a.split && a.sink != nullptr && h < hg) denom += exp2f(a.sink[h0 + h] * 1.4426950408889634f - m);
-          factor = 1.f / denom;
-        }
-        sh.fin[h] = factor;
-        if (h < hg) {
-          if (a.split) {
-            a.part_lse[(static_cast<int64_t>(slot) * a.T + t) * a.H + h0 + h] = lse2;
-          } else if (a.lse != nullptr) {
-            a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h0 + h] = lse2 * 0.6931471805599453f;
+          fw[h] = lsel > 0.f ? __frcp_rn(denom) : 0.f;
+          if (warp == 0 && h < hg) {
+            const float lse2 = lsel > 0.f ? m + log2f(lsel) : -INFINITY;
+            if (a.split) {
+              a.part_lse[(static_cast<int64_t>(slot) * a.T + t) * a.H + h0 + h] = lse2;
+            } else if (a.lse != nullptr) {
+              a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h0 + h] = lse2 * 0.6931471805599453f;
+            }
           }
         }
+        __syncwarp();
       }
-    }
-    if (!sm_sync(sh, smph)) return;
-    if (a.split) {
-      // partial O^T rows: thread tid writes channel 128b + tid of the group's heads as one
-      // contiguous run (heads padded to a multiple of 8 in the workspace layout)
-      uint16_t* prow = static_cast<uint16_t*>(a.part_o) +
-                       ((static_cast<int64_t>(slot) * a.T + t) * kDv + tid) * a.hp + h0;
-#pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < NH; c0 += CW) {
-          if (c0 >= hg) break;
-          float o[CW], f[CW];
-          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
+      float f[CW];
 #pragma unroll
-          for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
-          uint4* dst = reinterpret_cast<uint4*>(prow + static_cast<int64_t>(b) * 128 * a.hp + c0);
+      for (int i = 0; i < CW; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(fw + c0 + i);
+        f[i] = v.x;
+        f[i + 1] = v.y;
+        f[i + 2] = v.z;
+        f[i + 3] = v.w;
+      }
+      if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(249);
+      if (a.split) {
+        // partial O^T in head chunks of 8: entry (channel, 8 heads) of chunk k is 16 bytes at
+        // ((slot*T + t)*nchunks + k)*512 + channel, so a warp's 32 channels are 512 contiguous
+        // bytes per store
+        uint4* pbase = reinterpret_cast<uint4*>(a.part_o) +
+                       ((static_cast<int64_t>(slot) * a.T + t) * a.nchunks + ((h0 + c0) >> 3)) * kDv + tid;
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b) {
+          float o[CW];
+          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
+          if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
 #pragma unroll
           for (int g8 = 0; g8 < CW / 8; ++g8) {
             if (c0 + 8 * g8 < hg) {
@@ -991,27 +1040,25 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
                                                                 f[i + 1] != 0.f ? o[i + 1] * f[i + 1] : 0.f);
                 w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
               }
-              dst[g8] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              pbase[static_cast<int64_t>(g8) * kDv + 128 * b] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
           }
+          if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(251 + (b < 2 ? b : (b == 3 ? 2 : 5)));
         }
-      }
-    } else {
-      // final O: thread tid holds channel 128b + tid of every head. Within each group of 8 lanes
-      // an 8x8 transpose of the bf16 values (three exchange stages on pairs packed two to a
-      // word) gives every lane 8 consecutive channels of one head, stored as one 16-byte write
-      // (rows 16-byte aligned, strides multiples of 8).
-      uint16_t* obase = a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
-      const int64_t hstride = a.out_stride_h;
-      const int k8 = lane & 7;
+      } else {
+        // final O: thread tid holds channel 128b + tid of every head. Within each group of 8
+        // lanes an 8x8 transpose of the bf16 values (three exchange stages on pairs packed two
+        // to a word) gives every lane 8 consecutive channels of one head, stored as one 16-byte
+        // write (rows 16-byte aligned, strides multiples of 8).
+        uint16_t* obase =
+            a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
+        const int64_t hstride = a.out_stride_h;
+        const int k8 = lane & 7;
 #pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-#pragma unroll 1
-        for (int c0 = 0; c0 < NH; c0 += CW) {
-          float o[CW], f[CW];
+        for (int b = 0; b < 4; ++b) {
+          float o[CW];
           tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
-#pragma unroll
-          for (int i = 0; i < CW; ++i) f[i] = sh.fin[c0 + i];
+          if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
 #pragma unroll
           for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
 #pragma unroll
@@ -1066,9 +1113,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
             if (h < hg)
               *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) = make_uint4(p[0], p[1], p[2], p[3]);
           }
+          if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(251 + (b < 2 ? b : (b == 3 ? 2 : 5)));
         }
       }
+      if (tid == 0 && tr_first) SMLA_TRACE_AT(254);
     }
+    tr_first = false;
+    if (tid == 0) SMLA_TRACE_TILE(j, 9);
     tc_fence_before();
   }
 }
@@ -1077,6 +1128,7 @@ template <int NH, int F0, int F1>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_constant__ AttnArgs a) {
   using L = Smem<NH>;
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) SMLA_TRACE_AT(0);
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared sh;
   sh.base = base;
@@ -1139,6 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   // launched as a programmatic dependent of the previous kernel on the stream: the set-up above
   // overlaps its tail; nothing in global memory is read or written before it has completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) SMLA_TRACE_AT(1);
 
   if (warp < kSmWarps) {
     softmax_role<NH>(a, sh, tmem, lo, n);
@@ -1152,6 +1205,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem, TmemCols<NH>::kAlloc);
   }
+  if (threadIdx.x == 0) SMLA_TRACE_AT(2);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -1196,18 +1250,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     int c0;
     item_slots(a, t, hbase + 8 * g, c0, ns);
   }
-  const int64_t sstride = static_cast<int64_t>(a.T) * kDv * a.hp;
-  const uint16_t* col = static_cast<const uint16_t*>(a.part_o) +
-                        (static_cast<int64_t>(t) * kDv + cbase + (tid >> 2)) * a.hp + hbase + 8 * g;
+  // partial entry (channel, 8 heads) of head chunk k: 16 bytes at ((slot*T + t)*nchunks + k)*512 + channel
+  const int64_t sstride = static_cast<int64_t>(a.T) * a.nchunks * kDv;  // in 16-byte entries
+  const uint4* col = reinterpret_cast<const uint4*>(a.part_o) +
+                     (static_cast<int64_t>(t) * a.nchunks + ((hbase >> 3) + g)) * kDv + cbase + (tid >> 2);
   uint4 v[kCombineSlots][kChunks];
   auto issue = [&](int s0) {
 #pragma unroll
     for (int s = 0; s < kCombineSlots; ++s)
 #pragma unroll
       for (int q = 0; q < kChunks; ++q)
-        v[s][q] = s0 + s < ns ? *reinterpret_cast<const uint4*>(col + (s0 + s) * sstride +
-                                                                 static_cast<int64_t>(q) * kChStep * a.hp)
-                              : make_uint4(0, 0, 0, 0);
+        v[s][q] = s0 + s < ns ? col[(s0 + s) * sstride + q * kChStep] : make_uint4(0, 0, 0, 0);
   };
   issue(0);
 
@@ -1368,6 +1421,12 @@ cudaError_t launch_attention(const AttnArgs& args, const Plan& plan, cudaStream_
     default: return cudaErrorInvalidValue;
   }
 }
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_read(void* host, size_t bytes) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace)));
+}
+#endif
 
 cudaError_t read_and_clear_device_error(int* code) {
   int zero = 0;

@@ -1,0 +1,195 @@
+// Cache writer: packs new latent rows (512 latent + 64 rope values, bf16 or fp32) into the
+// paged cache in either row format, quantising to FP8 E4M3 with one fp32 scale per 128
+// latent channels. The pages name this step as the packing of their benchmark inputs
+// (flashinfer PR "add topk=256 prefill-dsv4 dispatch", conversation, GB10 benchmark "Method"
+// paragraph) without its arithmetic; per 128-channel block this kernel computes
+//   scale = amax / 448 (fp32, correctly rounded; 1 for an all-zero block)
+//   code  = E4M3FN(x / scale)  (fp32 quotient, round to nearest even, saturate to +-448)
+// and rounds rope channels (every channel of a bf16 row) to bf16, nearest even.
+//
+// One warp per row; lane l owns latent channels 16l..16l+15, so the eight lanes of a
+// 128-channel block find its amax with three shuffles and every store is a coalesced
+// 16-byte write. HBM-bound: a row reads 1152 (bf16) or 2304 (fp32) bytes and writes 656
+// (FP8) or 1152 (bf16) bytes.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "smla.h"
+#include "smla_internal.h"
+
+namespace smla {
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+struct QuantArgs {
+  const uint8_t* kv;
+  int64_t kv_stride_bytes;  // bytes between consecutive input rows
+  int32_t in_f32;           // 0: bf16 input, 1: fp32 input
+  int32_t n;
+  const int64_t* slots;
+  uint8_t* cache;
+  int64_t row_stride, page_stride;
+  int64_t num_slots;        // num_pages * 64
+  int32_t fp8;
+};
+
+__device__ __forceinline__ uint4 ldg_v4(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two E4M3FN codes (round to nearest even, saturating), a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// Two fp32 values -> two bf16 (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// This lane's 16 consecutive input values starting at channel c0, as fp32.
+__device__ __forceinline__ void load16(const QuantArgs& q, const uint8_t* row, int c0, float* x) {
+  if (q.in_f32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = ldg_v4(row + 4 * (c0 + 4 * k));
+      x[4 * k] = __uint_as_float(v.x);
+      x[4 * k + 1] = __uint_as_float(v.y);
+      x[4 * k + 2] = __uint_as_float(v.z);
+      x[4 * k + 3] = __uint_as_float(v.w);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 v = ldg_v4(row + 2 * (c0 + 8 * k));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * k + 2 * i] = bf16_lo(w[i]);
+        x[8 * k + 2 * i + 1] = bf16_hi(w[i]);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __grid_constant__ QuantArgs q) {
+  const int lane = threadIdx.x & 31;
+  const long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (i >= q.n) return;
+  const long long slot = q.slots[i];
+  if (slot < 0 || slot >= q.num_slots) return;
+  const uint8_t* in = q.kv + i * q.kv_stride_bytes;
+  uint8_t* out = q.cache + (slot >> 6) * q.page_stride + (slot & 63) * q.row_stride;
+
+  if (!q.fp8) {
+    // bf16 row: 576 channels = 72 chunks of 8 values
+    for (int ch = lane; ch < 72; ch += 32) {
+      uint4 o;
+      if (q.in_f32) {
+        const uint4 a = ldg_v4(in + 32 * ch);
+        const uint4 b = ldg_v4(in + 32 * ch + 16);
+        o = make_uint4(bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                       bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
+                       bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
+                       bf16x2(__uint_as_float(b.z), __uint_as_float(b.w)));
+      } else {
+        o = ldg_v4(in + 16 * ch);
+      }
+      *reinterpret_cast<uint4*>(out + 16 * ch) = o;
+    }
+    return;
+  }
+
+  // FP8 row: latent channels 16*lane .. 16*lane+15 belong to block lane/8
+  float x[16];
+  load16(q, in, 16 * lane, x);
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = e4m3x2(__fdiv_rn(x[4 * k], scale), __fdiv_rn(x[4 * k + 1], scale));
+    const uint32_t hi = e4m3x2(__fdiv_rn(x[4 * k + 2], scale), __fdiv_rn(x[4 * k + 3], scale));
+    w[k] = lo | (hi << 16);
+  }
+  *reinterpret_cast<uint4*>(out + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+  // the four block scales, gathered into lane 0 and stored as one 16-byte write
+  const float s1 = __shfl_sync(0xffffffffu, scale, 8);
+  const float s2 = __shfl_sync(0xffffffffu, scale, 16);
+  const float s3 = __shfl_sync(0xffffffffu, scale, 24);
+  if (lane == 0)
+    *reinterpret_cast<uint4*>(out + kDv) =
+        make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3));
+  // rope: 64 channels -> bf16, 8 lanes x 8 channels
+  if (lane < 8) {
+    uint4 o;
+    if (q.in_f32) {
+      const uint8_t* r = in + 4 * (kDv + 8 * lane);
+      const uint4 a = ldg_v4(r);
+      const uint4 b = ldg_v4(r + 16);
+      o = make_uint4(bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                     bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
+                     bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
+                     bf16x2(__uint_as_float(b.z), __uint_as_float(b.w)));
+    } else {
+      o = ldg_v4(in + 2 * (kDv + 8 * lane));
+    }
+    *reinterpret_cast<uint4*>(out + kDv + 16 + 16 * lane) = o;
+  }
+}
+
+}  // namespace
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" smla_status smla_quantize_kv(const void* kv, int32_t kv_dtype, int64_t kv_stride, int32_t n,
+                                        const int64_t* slots, void* cache, int32_t format,
+                                        int64_t row_stride_bytes, int64_t page_stride_bytes, int32_t num_pages,
+                                        smla_stream_t stream) {
+  if (n < 0 || (kv_dtype != SMLA_IN_BF16 && kv_dtype != SMLA_IN_F32)) return SMLA_ERR_INVALID;
+  if (format != SMLA_KV_BF16 && format != SMLA_KV_FP8_E4M3_S128) return SMLA_ERR_UNSUPPORTED;
+  if (n == 0) return SMLA_OK;
+  const int64_t esize = kv_dtype == SMLA_IN_F32 ? 4 : 2;
+  const int64_t row_bytes = format == SMLA_KV_BF16 ? kRowBf16 : kRowFp8;
+  if (kv == nullptr || slots == nullptr || cache == nullptr || num_pages < 1 || num_pages > kMaxPages)
+    return SMLA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(kv) & 15u) != 0 || (reinterpret_cast<uintptr_t>(cache) & 15u) != 0 ||
+      kv_stride < kDqk || ((kv_stride * esize) & 15) != 0)
+    return SMLA_ERR_INVALID;
+  if (row_stride_bytes < row_bytes || (row_stride_bytes & 15) != 0 || page_stride_bytes < kPage * row_stride_bytes ||
+      (page_stride_bytes & 15) != 0)
+    return SMLA_ERR_INVALID;
+  QuantArgs q{};
+  q.kv = static_cast<const uint8_t*>(kv);
+  q.kv_stride_bytes = kv_stride * esize;
+  q.in_f32 = kv_dtype == SMLA_IN_F32 ? 1 : 0;
+  q.n = n;
+  q.slots = slots;
+  q.cache = static_cast<uint8_t*>(cache);
+  q.row_stride = row_stride_bytes;
+  q.page_stride = page_stride_bytes;
+  q.num_slots = static_cast<int64_t>(num_pages) * kPage;
+  q.fp8 = format == SMLA_KV_FP8_E4M3_S128 ? 1 : 0;
+  const unsigned grid = static_cast<unsigned>((static_cast<long long>(n) + kQuantWarps - 1) / kQuantWarps);
+  quantize_kv_kernel<<<grid, kQuantWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    note_cuda_error(e, "launch of quantize_kv_kernel");
+    return SMLA_ERR_CUDA;
+  }
+  return SMLA_OK;
+}

@@ -16,6 +16,7 @@
 #include <atomic>
 
 #include "smla.h"
+#include "smla_internal.h"
 
 namespace {
 
@@ -33,12 +34,21 @@ std::atomic<void*> g_scratch_addr[kMaxDevices];
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (e != cudaSuccess) {
+    smla::note_cuda_error(e, "cudaGetDevice (smla_decode_static)");
+    return e;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    smla::note_cuda_error(cudaErrorInvalidDevice, "device index beyond the static scratch table");
+    return cudaErrorInvalidDevice;
+  }
   void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
   if (p == nullptr) {
     e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      smla::note_cuda_error(e, "cudaGetSymbolAddress(g_static_scratch)");
+      return e;
+    }
     g_scratch_addr[dev].store(p, std::memory_order_release);
   }
   *out = p;

@@ -202,8 +202,12 @@ def test_head_independence_on_gpu():
 
 # --------------------------------------------------------------------------- full-size configs
 def _sample(T, n, seed):
+    """n distinct tokens of T (seeded), always including the first and the last."""
     rng = np.random.default_rng(seed)
-    return np.sort(rng.choice(T, size=min(n, T), replace=False))
+    if n >= T:
+        return np.arange(T)
+    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
+    return np.sort(np.concatenate([[0, T - 1], mid]))
 
 
 @pytest.fixture(scope="module")
@@ -213,17 +217,18 @@ def config2():
 
 @pytest.mark.parametrize("mode", MODES)
 def test_config2_decode_full(oracle_mod, config2, mode):
-    parity(config2, mode, oracle_mod, tokens=_sample(config2.T, 16, 2))
+    # every token of the batch
+    parity(config2, mode, oracle_mod, tokens=_sample(config2.T, config2.T, 2))
 
 
 def test_config3_prefill_full(oracle_mod):
     w = synth.config(3)
-    parity(w, "forward", oracle_mod, tokens=_sample(w.T, 24, 3))
+    parity(w, "forward", oracle_mod, tokens=_sample(w.T, 96, 3))
 
 
 def test_config4_large_prefill_full(oracle_mod):
     w = synth.config(4)
-    parity(w, "forward", oracle_mod, tokens=_sample(w.T, 8, 4))
+    parity(w, "forward", oracle_mod, tokens=_sample(w.T, 72, 4))
 
 
 def test_sweep_points(oracle_mod):

@@ -59,6 +59,32 @@ def test_static_scratch_matches_workspace_decode(seed, T, H, topk):
         fin = np.isfinite(L_ref)
         assert np.array_equal(fin, np.isfinite(L)), call
         assert np.max(np.abs(L[fin] - L_ref[fin])) <= 1e-2, call
+        # the same plan and kernels run in both entry points: the bytes are identical
+        assert np.array_equal(O, O_ref) and np.array_equal(L, L_ref), call
+
+
+def test_static_scratch_against_the_oracle(oracle_mod):
+    w = synth.small_case(903, T=5, H=32, topk=1536, ctx=8192, fmt=synth.FMT_FP8, sink=True, mask_p=0.05)
+    dp = binding.DeviceProblem(w)
+    assert 0 < binding.workspace_size(dp.call) <= SCRATCH_LIMIT
+    for call in range(2):
+        assert binding.decode_static(dp.call) == binding.SMLA_OK
+        O, L = _outputs(dp)
+        O_ref, L_ref = oracle_mod.attention(w)
+        assert np.max(np.abs(O - O_ref)) <= TOL_FP8 * np.max(np.abs(O_ref)), call
+        assert np.max(np.abs(L - L_ref)) <= 1e-2, call
+
+
+def test_static_scratch_rejects_problems_beyond_its_size():
+    # T=1024 tokens of 128 heads on the split-K schedule need far more than 32 MiB of partials;
+    # the tensors are real and full-sized, so nothing could be read out of bounds in any case
+    w = synth.small_case(905, T=1024, H=128, topk=2048, ctx=4096, fmt=synth.FMT_FP8)
+    dp = binding.DeviceProblem(w)
+    assert binding.workspace_size(dp.call) > SCRATCH_LIMIT
+    dp.out.fill_(float("nan"))
+    assert binding.decode_static(dp.call, check=False) == binding.SMLA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.isnan(dp.out.float()).all()  # nothing was launched
 
 
 def test_static_scratch_validates_like_decode():

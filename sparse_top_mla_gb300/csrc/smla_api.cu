@@ -220,6 +220,7 @@ smla_status run(const smla_params* p, cudaStream_t stream, bool split_k) {
   if (st != SMLA_OK) return st;
   if (p->T == 0) return SMLA_OK;
   const Plan pl = make_plan(p, split_k);
+  if (pl.total_tiles >= (1ll << 31)) return SMLA_ERR_UNSUPPORTED;  // tile positions are 32-bit in the kernel
   if (pl.split) {
     if (p->workspace == nullptr || p->workspace_bytes < pl.workspace_bytes ||
         (reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)

@@ -20,10 +20,10 @@
 // block as the loaders refill the blocks PV has finished with.
 //
 // Softmax: P = 2^(s*scale*log2e - m) against per-head running maxima m. A tile whose scores
-// stay within 2^8 of the maxima (the common case) needs no cross-warp step: the warps write
-// P^T and arrive; the issuing thread checks a shared overflow flag and, only if it is set,
-// sends every softmax warp through the rescale pass (new maxima, O^T and L rescaled, P
-// recomputed) before it issues PV. The first tile of an item always takes the max pass.
+// stay within 2^8 of the maxima (the common case) needs one barrier among the softmax warps,
+// on which they learn whether any row overflowed; only then do they run the rescale pass (new
+// maxima, O^T and L rescaled, P recomputed) before PV is issued. The first tile of an item
+// always takes the max pass.
 //
 // Schedules: whole items per CTA (prefill; the epilogue writes O and LSE), or contiguous
 // flat tile ranges per CTA (split-K decode; every item segment writes a normalised partial
@@ -49,7 +49,7 @@ __device__ int g_device_error;
 // Event timestamps (global timer, ns) per CTA for timeline analysis; compiled in only with
 // -DSMLA_TRACE. Slot layout: 0 entry, 1 after the dependency wait, 2 exit, 3 first rows
 // published, 4 first loads issued; tile j < 24 at 8 + 10j: +0 S^T ready, +1 fast pass done,
-// +2 decision known, +3 PV issued, +4 blocks 0-3 stored (issuer), +5 blocks 4-8 stored
+// +2 P^T final (issuer), +3 PV issued, +4 blocks 0-3 stored (issuer), +5 blocks 4-8 stored
 // (issuer), +6/+7 the loaders' arrivals, +8/+9 epilogue start/end.
 #ifdef SMLA_TRACE
 __device__ unsigned long long g_trace[1024][256];
@@ -111,11 +111,9 @@ static_assert(Smem<64>::kAlloc <= 232448, "shared memory budget");
 constexpr int kBarFullA = 0;      // tile blocks 0-3 stored (8 loader warps arrive)
 constexpr int kBarFullB = 1;      // tile blocks 4-8 stored (8 loader warps arrive)
 constexpr int kBarSFull = 9;      // S^T of the tile is in TMEM (tcgen05.commit)
-constexpr int kBarPReady = 10;    // P^T in smem (4 softmax warps arrive)
 constexpr int kBarPvDone = 11;    // [4] PV block pair done (tcgen05.commit)
 constexpr int kBarRow = 15;       // [4] rows of tile j in slot j&3 (softmax warps 0-2 arrive)
 constexpr int kBarSm = 19;        // barrier among the 128 softmax threads (every thread arrives)
-constexpr int kBarDecision = 20;  // the issuing thread has read the overflow flag of the tile
 constexpr int kBarPFixed = 21;    // rescale pass done, P^T rewritten (4 softmax warps arrive)
 
 template <int NH>
@@ -137,26 +135,29 @@ struct Shared {
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   volatile int* rescale_flag;
-  volatile int* overflow;  // [2] a score of the tile passed its threshold (by tile parity)
-  volatile int* decision;  // [2] the tile takes the rescale pass (by tile parity)
+  volatile int* overflow;  // [2] tag j+1: a score of tile j passed its threshold (by tile parity)
   uint32_t ones;           // 128 B of bf16 1.0
   __device__ uint32_t bar(int i) const { return bars + 8u * i; }
 };
 
-// Bounded wait on an mbarrier phase. The thread sleeps in hardware between checks; only after
-// a sleep ends without the phase does it look at the abort flag and the clock.
-__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait on an mbarrier phase. The common case (phase already complete) is inline; the
+// waiting loop is one out-of-line copy: the thread sleeps in hardware between checks, and only
+// after a sleep ends without the phase does it look at the abort flag and the clock.
+__device__ __noinline__ bool wait_bar_slow(volatile int* abort_flag, uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
-    if (*sh.abort_flag) return false;
+    if (*abort_flag) return false;
     if (clock64() - t0 > kSpinCycles) {
       atomicExch(&g_device_error, kErrTimeout);
-      *sh.abort_flag = 1;
+      *abort_flag = 1;
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(sh.abort_flag, bar, parity);
 }
 
 // Warp-uniform wait: the warp proceeds only if all lanes saw the phase (a lane that gave up
@@ -865,7 +866,6 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   bool tr_first = true;  // first epilogue of the CTA (event timestamps only)
   (void)tr_first;
   int nfix = 0;  // rescale passes so far (phase of PFixed)
-  int ndec = 0;  // fast-pass decisions so far (phase of PReady and Decision, overflow/decision slot)
   if (n <= 0) return;
 
   // ---- index resolution, by warps 0-2 (warp 0 also takes rows 96-127, so the issuing warp
@@ -920,32 +920,20 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     tc_fence_after();
     if (tid == 0) SMLA_TRACE_TILE(j, 0);
     // the first tile of an item has no running maxima yet: it always takes the max pass, which
-    // every warp knows, so it skips the fast pass and the decision hand-shake
+    // every warp knows, so it skips the fast pass and the decision barrier
     bool fix = true;
     if (!first) {
       const bool over = p_pass<NH>(a, sh, tl + TC::kS, pt, valid, tid);
       if (tid == 0) SMLA_TRACE_TILE(j, 1);
-      if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[ndec & 1] = 1;
+      // decision among the four softmax warps: a warp with an overflowing row tags the tile's
+      // flag slot with j+1 (a tag, so no slot is ever reset); after the barrier every warp reads
+      // the same decision. A slot is written again two tiles later, after every warp has passed
+      // the next tile's barrier and therefore finished reading it.
+      if (__any_sync(0xffffffffu, over) && lane == 0) sh.overflow[j & 1] = j + 1;
       fence_proxy_async_smem();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sh.bar(kBarPReady));
-      // ---- decision: the issuing thread reads the overflow flag once all four warps arrived
-      if (warp == kIssueWarp) {
-        if (!wait_bar_w(sh, sh.bar(kBarPReady), ndec & 1)) return;
-        int f = 0;
-        if (lane == 0) {
-          f = sh.overflow[ndec & 1];
-          sh.overflow[ndec & 1] = 0;
-          sh.decision[ndec & 1] = f;
-          mbar_arrive(sh.bar(kBarDecision));
-        }
-        fix = __shfl_sync(0xffffffffu, f, 0) != 0;
-      } else {
-        if (!wait_bar_w(sh, sh.bar(kBarDecision), ndec & 1)) return;
-        fix = sh.decision[ndec & 1] != 0;
-      }
-      ++ndec;
+      if (!sm_sync(sh, smph)) return;
+      fix = sh.overflow[j & 1] == j + 1;
     }
     if (fix) {
       if (!max_pass<NH>(a, sh, tl, pt, valid, first, smph, tid)) return;
@@ -957,6 +945,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     if (warp == kIssueWarp) {
       if (fix && !wait_bar_w(sh, sh.bar(kBarPFixed), nfix & 1)) return;
       if (lane == 0) SMLA_TRACE_TILE(j, 2);
+      tc_fence_after();
       if (!mma_issue_after<NH>(sh, tmem, j, n, first)) return;
     }
     if (fix) ++nfix;
@@ -1148,7 +1137,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   sh.abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
   sh.rescale_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 8);
   sh.overflow = reinterpret_cast<volatile int*>(base + L::kMiscOff + 16);
-  sh.decision = reinterpret_cast<volatile int*>(base + L::kMiscOff + 24);
   sh.ones = smem_u32(base + L::kOnesOff);
 
   const int warp = threadIdx.x >> 5;
@@ -1166,16 +1154,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     mbar_init(sh.bar(kBarFullA), kLdWarps);
     mbar_init(sh.bar(kBarFullB), kLdWarps);
     mbar_init(sh.bar(kBarSFull), 1);
-    mbar_init(sh.bar(kBarPReady), kSmWarps);
     mbar_init(sh.bar(kBarSm), kSmWarps * 32);
-    mbar_init(sh.bar(kBarDecision), 1);
     mbar_init(sh.bar(kBarPFixed), kSmWarps);
     for (int i = 0; i < 4; ++i) mbar_init(sh.bar(kBarPvDone + i), 1);
     for (int i = 0; i < 4; ++i) mbar_init(sh.bar(kBarRow + i), kIssueWarp);
     *sh.abort_flag = 0;
     *sh.rescale_flag = 0;
     sh.overflow[0] = sh.overflow[1] = 0;
-    sh.decision[0] = sh.decision[1] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(base + L::kOnesOff)[threadIdx.x] = 0x3F803F80u;

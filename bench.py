@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse-MLA prefill TFLOP/s & decode µs/call + GB/s, as % of roofline"
 ROTATIONS = 8
 # about half a second of timed GPU work per workload
-DEFAULT_STEPS = {"decode": 6000, "prefill": 800, "large_prefill": 40, "tiny": 8000}
+DEFAULT_STEPS = {"decode": 6000, "prefill": 800, "large_prefill": 40, "tiny": 8000, "quantize": 200}
 
 
 def parse():
@@ -50,9 +50,11 @@ def parse():
                          "20 ms clock samples fall inside the timed region)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny", "quantize"])
     ap.add_argument("--no-secondary", action="store_true",
-                    help="decode only: leave the prefill and large-prefill workloads out of the line")
+                    help="decode only: leave the prefill, large-prefill and cache-writer workloads out of the line")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="prefill / large_prefill: time only the first N query tokens (smaller profiler captures)")
     args = ap.parse_args()
     args.steps_given = args.steps > 0
     if args.steps <= 0:
@@ -95,8 +97,9 @@ def max_over_ranks(x, world):
 
 
 # ----------------------------------------------------------------------------- workloads
-def build_workloads(kind):
+def build_workloads(kind, tokens=0):
     from sparse_top_mla_gb300 import synth
+    T = tokens if tokens > 0 else None
     if kind == "decode":
         base = synth.config(2)
         rots = [base]
@@ -107,11 +110,13 @@ def build_workloads(kind):
             rots.append(synth.replace(base, q=q, main=synth.replace(base.main, indices=idx)))
         return rots, "decode fp8: 64 seqs x 16384 ctx (688 MB cache), T=64, H=64, topk=2048 (5% -1), sink"
     if kind == "prefill":
-        return [synth.config(3)], "prefill bf16: 1 seq x 32768 ctx, T=4096, H=32, topk=512 causal, sink"
+        w = synth.config(3, T=T)
+        return [w], f"prefill bf16: 1 seq x 32768 ctx, T={w.T}, H=32, topk=512 causal, sink"
     if kind == "tiny":
         return [synth.config(1)], "tiny bf16: 1 seq x 256 ctx, T=4, H=16, topk=128, no sink"
-    return [synth.config(4)], ("large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T=8192, H=128, "
-                               "topk=2048 causal + 128-token window, sink")
+    w = synth.config(4, T=T)
+    return [w], (f"large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T={w.T}, H=128, "
+                 "topk=2048 causal + 128-token window, sink")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -237,6 +242,26 @@ def run_reference(args, world, rank):
     import oracle
     from sparse_top_mla_gb300 import synth
     oracle.build()
+    if args.workload == "quantize":
+        rng = np.random.default_rng(3000)
+        x = synth.f32_to_bf16_bits(synth.normal_f32(rng, (65536, 576)))
+        times = []
+        for s in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.pack_rows(x, 1)
+            if s >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        gbs = x.shape[0] * (1152 + 656 + 8) * len(times) / sum(times) / 1e9
+        sample = "65536 bf16 latent rows per step (of the 1,048,576-row cache), fp64 oracle cache writer"
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": sum(times) / len(times) * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                          "data": "synthetic", "config": {"workload": "cache writer", "sample": sample},
+                          "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.threads(0), "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                          "gpu_launches": 0}), flush=True)
+        return 0
     w = {"decode": lambda: synth.config(2), "prefill": lambda: synth.config(3), "tiny": lambda: synth.config(1),
          "large_prefill": lambda: synth.config(4, T=64)}[args.workload]()
     per_tok = w.gathered_bytes() / w.T
@@ -265,12 +290,12 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- smla arm
-def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True):
+def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens=0):
     import torch
     from sparse_top_mla_gb300 import binding
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    rots, label = build_workloads(kind)
+    rots, label = build_workloads(kind, tokens)
     probs = [binding.DeviceProblem(rots[0], device=dev)]
     # the other rotations share the first rotation's device cache (only q and indices differ)
     for w in rots[1:]:
@@ -357,38 +382,101 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True):
     if not with_e2e:
         return res
 
-    # e2e: pinned host inputs -> device, forward, outputs -> pinned host, every step
-    h_q = [torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory() for w in rots]
-    h_idx = [torch.from_numpy(np.ascontiguousarray(w.main.indices)).pin_memory() for w in rots]
-    h_meta = [torch.from_numpy(np.concatenate([w.token_seq, w.main.seq_lens, w.main.block_table.reshape(-1)]))
-              .pin_memory() for w in rots]
-    h_sink = [torch.from_numpy(w.sink).pin_memory() if w.sink is not None else None for w in rots]
-    h_out = torch.empty((w0.T, w0.H, 512), dtype=torch.int16).pin_memory()
-    h_lse = torch.empty((w0.T, w0.H), dtype=torch.float32).pin_memory()
-    h2d = h_q[0].numel() * 2 + h_idx[0].numel() * 4 + h_meta[0].numel() * 4 + (h_sink[0].numel() * 4 if h_sink[0]
-                                                                                 is not None else 0)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    # e2e: pinned host inputs -> device, forward, outputs -> pinned host, every step. Each
+    # step's inputs (q, indices, token_seq, seq_lens, block table, sink) sit packed in one pinned
+    # host buffer and are uploaded with one copy into one device buffer the call's tensors view;
+    # O and LSE come back with one copy. The copies run on their own streams so they overlap the
+    # kernels of neighbouring steps, as in a serving loop: uploads of step s on the input stream,
+    # the forward on the compute stream once they have landed, the download of step s on the
+    # output stream once it is done. Every rotation has its own device buffers, rewritten only
+    # after its previous forward and download completed (events); host output buffers alternate.
+    def packed(parts):
+        offs, n = [], 0
+        for a in parts:
+            offs.append(n)
+            n += (a.nbytes + 255) // 256 * 256
+        return offs, n
+
+    T, S = w0.T, w0.num_seqs
+    e_calls, d_in, h_in, d_out = [], [], [], []
+    for r, w in enumerate(rots):
+        ex = w.extra
+        arrs = [np.ascontiguousarray(w.q), np.ascontiguousarray(w.main.indices),
+                np.ascontiguousarray(w.token_seq, dtype=np.int32), np.ascontiguousarray(w.main.seq_lens),
+                np.ascontiguousarray(w.main.block_table),
+                np.ascontiguousarray(w.sink) if w.sink is not None else np.zeros(0, np.float32)]
+        if ex is not None:
+            arrs += [np.ascontiguousarray(ex.indices), np.ascontiguousarray(ex.seq_lens),
+                     np.ascontiguousarray(ex.block_table)]
+        offs, n = packed(arrs)
+        host = torch.zeros(n, dtype=torch.uint8).pin_memory()
+        for a, o in zip(arrs, offs):
+            host[o:o + a.nbytes].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+        dbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+
+        def view(i, dtype, shape):
+            return dbuf[offs[i]:offs[i] + arrs[i].nbytes].view(dtype).view(shape)
+
+        oo, on = packed([np.empty((T, w.H, 512), np.uint16), np.empty((T, w.H), np.float32)])
+        obuf = torch.empty(on, dtype=torch.uint8, device=dev)
+        main = binding.DeviceSet(probs[0].main.cache, w.main.fmt, w.main.row_stride, w.main.page_stride,
+                                 w.main.num_pages, view(4, torch.int32, w.main.block_table.shape),
+                                 view(3, torch.int32, w.main.seq_lens.shape), view(1, torch.int32, w.main.indices.shape),
+                                 w.main.topk)
+        extra = None
+        if ex is not None:
+            extra = binding.DeviceSet(probs[0].extra.cache, ex.fmt, ex.row_stride, ex.page_stride, ex.num_pages,
+                                      view(8, torch.int32, ex.block_table.shape), view(7, torch.int32, ex.seq_lens.shape),
+                                      view(6, torch.int32, ex.indices.shape), ex.topk)
+        call = binding.Call(view(0, torch.bfloat16, w.q.shape), view(2, torch.int32, (T,)), main,
+                            obuf[oo[0]:oo[0] + T * w.H * 1024].view(torch.bfloat16).view(T, w.H, 512),
+                            obuf[oo[1]:oo[1] + T * w.H * 4].view(torch.float32).view(T, w.H), extra,
+                            view(5, torch.float32, w.sink.shape) if w.sink is not None else None,
+                            np.float32(w.sm_scale), None, num_seqs=w.num_seqs)
+        call.set_workspace(probs[0].workspace)
+        e_calls.append(call)
+        d_in.append(dbuf)
+        h_in.append(host)
+        d_out.append(obuf)
+    h_out2 = [torch.empty(d_out[0].numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    h2d = h_in[0].numel()
+    d2h = d_out[0].numel()
     e2e_steps = min(steps, 20)
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    nrot = len(e_calls)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    up_done = [ev() for _ in range(e2e_steps)]
+    fwd_done = [ev() for _ in range(e2e_steps)]
+    down_done = [ev() for _ in range(e2e_steps)]
+    for c in e_calls[:1]:  # one untimed pass through this path
+        d_in[0].copy_(h_in[0])
+        binding.forward(c, stream)
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
     for s in range(e2e_steps):
-        r = s % len(probs)
-        p = probs[r]
-        p.q.view(torch.int16).copy_(h_q[r].view(p.q.shape), non_blocking=True)
-        p.main.indices.copy_(h_idx[r], non_blocking=True)
-        meta = h_meta[r]
-        T, S = w0.T, w0.num_seqs
-        p.token_seq.copy_(meta[:T], non_blocking=True)
-        p.main.seq_lens.copy_(meta[T:T + S], non_blocking=True)
-        p.main.block_table.view(-1).copy_(meta[T + S:], non_blocking=True)
-        if h_sink[r] is not None:
-            p.sink.copy_(h_sink[r], non_blocking=True)
-        binding.forward(p.call, stream)
-        h_out.copy_(p.out.view(torch.int16), non_blocking=True)
-        h_lse.copy_(p.lse, non_blocking=True)
+        r = s % nrot
+        with torch.cuda.stream(s_in):
+            if s >= nrot:
+                s_in.wait_event(fwd_done[s - nrot])  # the rotation's previous forward read its inputs
+            d_in[r].copy_(h_in[r], non_blocking=True)
+            up_done[s].record(s_in)
+        stream.wait_event(up_done[s])
+        if s >= nrot:
+            stream.wait_event(down_done[s - nrot])  # the rotation's previous outputs were read back
+        binding.forward(e_calls[r], stream)
+        fwd_done[s].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(fwd_done[s])
+            h_out2[s & 1].copy_(d_out[r], non_blocking=True)
+            down_done[s].record(s_out)
+    stream.wait_event(down_done[e2e_steps - 1])
+    stream.wait_event(up_done[e2e_steps - 1])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -498,6 +586,52 @@ def line_for(kind, r, args, world, cpu):
     return d
 
 
+def time_quantize(steps, warmup, world, local):
+    """The device cache writer over the decode cache: 64 x 16384 rows of bf16 latents (1.2 GB)
+    packed into FP8 rows (688 MB) at shuffled physical slots. HBM-bound: every row reads 1152
+    bytes and writes 656."""
+    import torch
+    from sparse_top_mla_gb300 import binding, synth
+    dev = torch.device(f"cuda:{local}")
+    n = 64 * 16384
+    rng = np.random.default_rng(3000)
+    # bf16 latents ~N(0,1), drawn in chunks by the seeded generator
+    kv = torch.empty((n, 576), dtype=torch.bfloat16, device=dev)
+    chunk = 65536
+    for c0 in range(0, n, chunk):
+        x = synth.normal_f32(rng, (chunk, 576))
+        kv[c0:c0 + chunk].view(torch.int16).copy_(torch.from_numpy(synth.f32_to_bf16_bits(x).view(np.int16)))
+    slots = torch.from_numpy(rng.permutation(n).astype(np.int64)).to(dev)
+    cache = torch.empty(n * 656, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        binding.quantize_kv(kv, slots, cache, 1, 656, 64 * 656, n // 64, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    before = ClockSampler.once(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        binding.quantize_kv(kv, slots, cache, 1, 656, 64 * 656, n // 64, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    after = ClockSampler.once(local)
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    peaks = measured_peaks()
+    alg = n * (1152 + 656 + 8)  # bf16 row in, fp8 row out, slot id
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"workload": "cache writer: 1,048,576 bf16 latent rows -> FP8 rows (656 B) at shuffled slots",
+            "value": gbs * world, "unit": "GB/s", "us_per_call": ms * 1e3, "steps": steps,
+            "rows_per_call": n, "l2": "inputs larger than L2: 1.2 GB of bf16 rows in, 688 MB of FP8 rows out",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic("quantize_kv"),
+                         "algorithmic_bytes_per_launch": alg, "kernel": "quantize_kv_kernel",
+                         "peak_source": peaks["source"] + " (hbm_gbs, STREAM-style copy)"},
+            "clocks": ClockSampler.summarise([], None, None, (before, after)), "gpu_launches": steps}
+
+
 def secondary_for(kind, r, cpu):
     """The prefill-type workload as a sub-object of the decode line (TFLOP/s headline)."""
     us = r["ms_per_step"] * 1e3
@@ -525,7 +659,17 @@ def main():
     if rank == 0:
         smla_build.build()
     barrier(world)
-    r = time_workload(args.workload, args.steps, args.warmup, world, rank, local, True)
+    if args.workload == "quantize":
+        qr = time_quantize(args.steps, args.warmup, world, local)
+        if rank == 0:
+            line = {"metric": METRIC, "value": qr["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                    "warmup": args.warmup, "ms_per_step": qr["us_per_call"] / 1e3, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
+                    "config": {"workload": qr["workload"], "l2": qr["l2"]}, "roofline": qr["roofline"],
+                    "clocks": qr["clocks"], "gpu_launches": qr["gpu_launches"]}
+            print(json.dumps(line), flush=True)
+        return 0
+    r = time_workload(args.workload, args.steps, args.warmup, world, rank, local, True, args.tokens)
     cpu = cpu_baseline_decode() if (rank == 0 and world == 1 and args.workload == "decode") else None
     line = line_for(args.workload, r, args, world, cpu)
     if args.workload == "decode" and not args.no_secondary:
@@ -533,12 +677,15 @@ def main():
         # number of steps when --steps is given, else for its own default (about half a second)
         for kind, n_tok in (("prefill", 256), ("large_prefill", 16)):
             steps = args.steps if args.steps_given else DEFAULT_STEPS[kind]
-            rr = time_workload(kind, steps, args.warmup, world, rank, local, False)
+            rr = time_workload(kind, steps, args.warmup, world, rank, local, False, args.tokens)
             cpu_k = cpu_baseline_tokens(kind, n_tok) if (rank == 0 and world == 1) else None
             line["config"][kind] = secondary_for(kind, rr, cpu_k)
             line["gpu_launches"] += rr["launches"]
             import torch
             torch.cuda.empty_cache()
+        qsteps = args.steps if args.steps_given else 200
+        line["config"]["quantize_kv"] = time_quantize(qsteps, args.warmup, world, local)
+        line["gpu_launches"] += qsteps
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

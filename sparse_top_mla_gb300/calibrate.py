@@ -60,21 +60,30 @@ def table_json(entries, meta: dict) -> str:
     return head + "".join(",\n" + l for l in lines) + "\n}\n"
 
 
-def _time_us(fn, calls, stream, reps: int) -> float:
+def _time_us(fn, calls, stream, reps: int, inner: int = 4) -> float:
+    """GPU time per call, from a CUDA graph replaying `inner` rounds of the rotating calls (the
+    pages' protocol times graph replays, GPU-only): host submission is then not part of the
+    number, which matters at small T where a call is a few microseconds of GPU work."""
     import torch
     for c in calls:
         fn(c, stream)
     stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(inner):
+            for c in calls:
+                fn(c, None)  # None: torch's current stream, the capture stream here
+    g.replay()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     best = math.inf
     for _ in range(reps):
         e0.record(stream)
-        for c in calls:
-            fn(c, stream)
+        g.replay()
         e1.record(stream)
         e1.synchronize()
-        best = min(best, e0.elapsed_time(e1) * 1e3 / len(calls))
+        best = min(best, e0.elapsed_time(e1) * 1e3 / (inner * len(calls)))
     return best
 
 
@@ -139,6 +148,7 @@ def calibrate(formats=(1,), heads=None, topks=None, t_grid=T_GRID, rotations: in
     meta = {"device": props.name, "sm_count": props.multi_processor_count,
             "rule": f"decode iff t_decode <= {ratio} t_prefill at T and every smaller grid T",
             "t_grid": list(t_grid), "rotations": rotations,
+            "timing": "CUDA-graph replay of 4 rounds of the rotating calls, best of reps, GPU time per call",
             "context": "64 sequences x 16384 tokens, random distinct indices, 5% masked, per-head sink",
             "timings_us_T_decode_prefill": timings}
     return {"entries": entries, "meta": meta}

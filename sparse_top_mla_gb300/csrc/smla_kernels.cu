@@ -36,6 +36,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 
@@ -1329,15 +1330,41 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   }
 }
 
-template <int NH, int F0, int F1>
-cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
-  const int smem = Smem<NH>::kAlloc;
-  cudaError_t e =
-      cudaFuncSetAttribute(sparse_mla_kernel<NH, F0, F1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+// Dynamic shared memory above 48 KB is enabled once per kernel and device (a bit per device in
+// `done`, for up to 64 devices; beyond that it is set on every call). `bytes_done` remembers the
+// largest size enabled so far for kernels whose request varies.
+template <typename K>
+cudaError_t enable_smem(K kernel, int bytes, std::atomic<uint64_t>& done, std::atomic<int>& bytes_done,
+                        const char* what) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 64;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0 && bytes <= bytes_done.load()) return cudaSuccess;
+  const int want = bytes > bytes_done.load() ? bytes : bytes_done.load();
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
   if (e != cudaSuccess) {
-    note_cuda_error(e, "cudaFuncSetAttribute(sparse_mla_kernel, max dynamic shared memory)");
+    note_cuda_error(e, what);
     return e;
   }
+  int prev = bytes_done.load();
+  while (want > prev && !bytes_done.compare_exchange_weak(prev, want)) {
+  }
+  if (bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+// one record for the combine kernel, which every attention instantiation launches
+std::atomic<uint64_t> g_combine_attr_done{0};
+std::atomic<int> g_combine_attr_bytes{0};
+
+template <int NH, int F0, int F1>
+cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
+  static std::atomic<uint64_t> attr_done{0};
+  static std::atomic<int> attr_bytes{0};
+  const int smem = Smem<NH>::kAlloc;
+  cudaError_t e = enable_smem(sparse_mla_kernel<NH, F0, F1>, smem, attr_done, attr_bytes,
+                              "cudaFuncSetAttribute(sparse_mla_kernel, max dynamic shared memory)");
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl;
   pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -1367,12 +1394,9 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
     cfg.gridDim = dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads, kCombineHalves);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
-    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(cfg.dynamicSmemBytes));
-    if (e != cudaSuccess) {
-      note_cuda_error(e, "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)");
-      return e;
-    }
+    e = enable_smem(combine_kernel, static_cast<int>(cfg.dynamicSmemBytes), g_combine_attr_done,
+                    g_combine_attr_bytes, "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)");
+    if (e != cudaSuccess) return e;
     cfg.stream = stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;

@@ -110,12 +110,14 @@ static_assert(Smem<64>::kAlloc <= 232448, "shared memory budget");
 
 // barrier indices
 constexpr int kBarFullA = 0;      // tile blocks 0-3 stored (8 loader warps arrive)
-constexpr int kBarFullB = 1;      // tile blocks 4-8 stored (8 loader warps arrive)
+constexpr int kBarFullB = 1;      // tile blocks 4-7 stored (8 loader warps arrive)
+constexpr int kBarFullR = 2;      // tile block 8 (rope) stored (8 loader warps arrive)
 constexpr int kBarSFull = 9;      // S^T of the tile is in TMEM (tcgen05.commit)
 constexpr int kBarPvDone = 11;    // [4] PV block pair done (tcgen05.commit)
 constexpr int kBarRow = 15;       // [4] rows of tile j in slot j&3 (softmax warps 0-2 arrive)
 constexpr int kBarSm = 19;        // barrier among the 128 softmax threads (every thread arrives)
 constexpr int kBarPFixed = 21;    // rescale pass done, P^T rewritten (4 softmax warps arrive)
+constexpr int kBarRowsum = 22;    // row sums (issued after the last PV block pair) done (tcgen05.commit)
 
 template <int NH>
 struct TmemCols {
@@ -598,25 +600,28 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
-      if (u == 0 && j == 2 && bp == 2) SMLA_TRACE_AT(5);
-      if (u == 0 && j == 2 && bp == 3) SMLA_TRACE_AT(7);
       if (bp == 0 && first && j > 0) load_q(cur.item);
       if (fmt_cur == 1) {
         ld_store_fp8<bp>(sh, rg, lane8, bp, D, dq);
       } else {
         ld_store_bf16<(bp & 1)>(sh, rg, lane8, bp, D);
       }
-      if (bp == 3) {
-#pragma unroll
-        for (int k = 0; k < kLdRows; ++k) sts_v4(sh.tile + 8 * kBlockBytes + swz(rg + 32 * k, lane8), D.rope[k]);
-      }
-      if (u == 0 && j == 2 && bp == 2) SMLA_TRACE_AT(6);
       if (bp == 0 && first) cp_async_wait_all();
-      if (bp & 1) {  // blocks 0-3 (after bp 1) or 4-8 (after bp 3) complete
+      if (bp & 1) {  // blocks 0-3 (after bp 1) or 4-7 (after bp 3) complete
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(sh.bar(bp == 1 ? kBarFullA : kBarFullB));
         if (u == 0) SMLA_TRACE_TILE(j, bp == 1 ? 6 : 7);
+      }
+      if (bp == 3) {
+        // the rope block holds the previous tile's P^T until its row sums (issued after the
+        // last PV block pair) have read it
+        if (j > 0 && !wait_bar_w(sh, sh.bar(kBarRowsum), (j - 1) & 1)) return false;
+#pragma unroll
+        for (int k = 0; k < kLdRows; ++k) sts_v4(sh.tile + 8 * kBlockBytes + swz(rg + 32 * k, lane8), D.rope[k]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sh.bar(kBarFullR));
       }
       // first tile: an fp8 tile's first refill already needs the next rows; a bf16 tile's
       // first refills still read the current tile
@@ -690,8 +695,8 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 0);
 #pragma unroll
   for (int kb = 0; kb < kKBlocks; ++kb) {
-    if (kb == 0 || kb == 4) {
-      if (!wait_bar_w(sh, sh.bar(kb == 0 ? kBarFullA : kBarFullB), j & 1)) return false;
+    if (kb == 0 || kb == 4 || kb == 8) {
+      if (!wait_bar_w(sh, sh.bar(kb == 0 ? kBarFullA : (kb == 4 ? kBarFullB : kBarFullR)), j & 1)) return false;
       tc_fence_after();
       if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, kb == 0 ? 4 : 5);
     }
@@ -738,17 +743,17 @@ __device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem)
 }
 
 // After the softmax of tile j: PV of all four block pairs (each with its own commit, so the
-// loaders refill a block pair as soon as it is released) and the row sums (before the last
-// block pair, so its commit covers them), then QK^T of tile j+1 as its blocks arrive.
+// loaders refill a block pair as soon as it is released), then the row sums with their own
+// commit (the loaders store the next rope block, where this tile's P^T lives, after it), then
+// QK^T of tile j+1 as its blocks arrive.
 template <int NH>
 __device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem, int j, int n, bool first) {
   const MmaDesc d = make_descs<NH>(sh);
   tc_fence_after();
 #pragma unroll 1
-  for (int bp = 0; bp < 4; ++bp) {
-    if (bp == 3) mma_rowsum<NH>(d, tmem, first);
-    mma_pv<NH>(sh, d, tmem, bp, first);
-  }
+  for (int bp = 0; bp < 4; ++bp) mma_pv<NH>(sh, d, tmem, bp, first);
+  mma_rowsum<NH>(d, tmem, first);
+  mma_commit_warp(sh.bar(kBarRowsum));
   if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, 3);
   if (j + 1 >= n) return true;
   if (!mma_qk<NH>(sh, d, tmem, j + 1)) return false;
@@ -956,7 +961,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
     // L holds the same row sums, so each warp derives the output factors of the heads it writes
     // from its own lanes: no step across warps (the issuing warp may still be queueing the next
     // tile's QK^T while the other warps write). Warp 0 also writes the LSEs.
-    if (!wait_bar_w(sh, sh.bar(kBarPvDone + 3), j & 1)) return;
+    if (!wait_bar_w(sh, sh.bar(kBarRowsum), j & 1)) return;
     tc_fence_after();
     if (tid == 0) SMLA_TRACE_TILE(j, 8);
     const uint32_t t = item_token(a, cur.item);
@@ -1154,6 +1159,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(kBarFullA), kLdWarps);
     mbar_init(sh.bar(kBarFullB), kLdWarps);
+    mbar_init(sh.bar(kBarFullR), kLdWarps);
+    mbar_init(sh.bar(kBarRowsum), 1);
     mbar_init(sh.bar(kBarSFull), 1);
     mbar_init(sh.bar(kBarSm), kSmWarps * 32);
     mbar_init(sh.bar(kBarPFixed), kSmWarps);

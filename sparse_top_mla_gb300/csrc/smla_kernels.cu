@@ -666,20 +666,23 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
 }
 
 // ------------------------------------------------------------------ MMA issue (one thread)
-// Descriptors are built once per call; each MMA adds a compile-time byte offset (>> 4) to the
-// start address field, so issuing costs a few instructions per MMA.
+// Descriptor low words are built once per call; each MMA adds a compile-time byte offset (>> 4)
+// to the start address field. The high words are constants of the operand layouts.
 struct MmaDesc {
-  uint64_t qk_a, qk_b, pv_a, pv_b, ones;
+  uint32_t qk_a, qk_b, pv_a, pv_b, ones;
 };
+constexpr uint32_t kHiK128 = smem_desc_hi(1024, kSwizzle128B);  // K-major, 128B swizzle, 8-row groups 1 KB apart
+constexpr uint32_t kHiP = smem_desc_hi(2048, kSwizzleNone);     // P^T: 8x8 core matrices, N groups 2 KB apart
+constexpr uint32_t kHiOnes = smem_desc_hi(0, kSwizzleNone);     // the ones operand: every group the same 128 B
 
 template <int NH>
 __device__ __forceinline__ MmaDesc make_descs(const Shared& sh) {
   MmaDesc d;
-  d.qk_a = smem_desc(sh.tile, 16, 1024, kSwizzle128B);
-  d.qk_b = smem_desc(sh.q, 16, 1024, kSwizzle128B);
-  d.pv_a = smem_desc(sh.tile, kBlockBytes, 1024, kSwizzle128B);
-  d.pv_b = smem_desc(sh.tile + 8 * kBlockBytes, 128, 2048, kSwizzleNone);
-  d.ones = smem_desc(sh.ones, 0, 0, kSwizzleNone);  // every row and K step reads the same ones
+  d.qk_a = smem_desc_lo(sh.tile, 16);
+  d.qk_b = smem_desc_lo(sh.q, 16);
+  d.pv_a = smem_desc_lo(sh.tile, kBlockBytes);
+  d.pv_b = smem_desc_lo(sh.tile + 8 * kBlockBytes, 128);
+  d.ones = smem_desc_lo(sh.ones, 0);  // every row and K step reads the same ones
   return d;
 }
 
@@ -700,10 +703,9 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
       tc_fence_after();
       if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, kb == 0 ? 4 : 5);
     }
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16_ss_warp(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint64_t>((kb * kBlockBytes + ks * 32) >> 4),
-                       d.qk_b + static_cast<uint64_t>((kb * NH * 128 + ks * 32) >> 4), idesc, (kb | ks) != 0);
+    // four K steps of 16 channels: 32 bytes along the swizzled row of block kb
+    mma_bf16_x4<2, 2>(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint32_t>((kb * kBlockBytes) >> 4), kHiK128,
+                      d.qk_b + static_cast<uint32_t>((kb * NH * 128) >> 4), kHiK128, idesc, kb != 0);
   }
   return true;
 }
@@ -713,11 +715,10 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
 template <int NH>
 __device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint32_t tmem, int bp, bool first) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 1, 1);
-  const uint64_t da = d.pv_a + static_cast<uint64_t>((2 * bp * kBlockBytes) >> 4);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    mma_bf16_ss_warp(tmem + TmemCols<NH>::kO + bp * NH, da + static_cast<uint64_t>((ks * 2048) >> 4),
-                     d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc, (first && ks == 0) ? 0u : 1u);
+  const uint32_t da = d.pv_a + static_cast<uint32_t>((2 * bp * kBlockBytes) >> 4);
+  // eight K steps of 16 tokens: 2 KB of V^T rows, 256 B of P^T core matrices per step
+  mma_bf16_x4<128, 16>(tmem + TmemCols<NH>::kO + bp * NH, da, kHiK128, d.pv_b, kHiP, idesc, first ? 0u : 1u);
+  mma_bf16_x4<128, 16>(tmem + TmemCols<NH>::kO + bp * NH, da + 512, kHiK128, d.pv_b + 64, kHiP, idesc, 1u);
   mma_commit_warp(sh.bar(kBarPvDone + bp));
 }
 
@@ -727,10 +728,8 @@ __device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint3
 template <int NH>
 __device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 1);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    mma_bf16_ss_warp(tmem + TmemCols<NH>::kL, d.ones, d.pv_b + static_cast<uint64_t>((ks * 256) >> 4), idesc,
-                     (first && ks == 0) ? 0u : 1u);
+  mma_bf16_x4<0, 16>(tmem + TmemCols<NH>::kL, d.ones, kHiOnes, d.pv_b, kHiP, idesc, first ? 0u : 1u);
+  mma_bf16_x4<0, 16>(tmem + TmemCols<NH>::kL, d.ones, kHiOnes, d.pv_b + 64, kHiP, idesc, 1u);
 }
 
 // QK^T of the first tile of the stream.
@@ -1124,11 +1123,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   using L = Smem<NH>;
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) SMLA_TRACE_AT(0);
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1 KB alignment computed on the 32-bit shared address (the MMA descriptors derive from it)
+  const uint32_t sraw = smem_u32(smem_raw);
+  const uint32_t s0 = (sraw + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (s0 - sraw);
   Shared sh;
   sh.base = base;
-  sh.tile = smem_u32(base);
-  sh.q = smem_u32(base + L::kQOff);
+  sh.tile = s0;
+  sh.q = s0 + L::kQOff;
   sh.red = reinterpret_cast<float*>(base + L::kRedOff);
   sh.m_run = reinterpret_cast<float*>(base + L::kMOff);
   sh.m_use = reinterpret_cast<float*>(base + L::kMUseOff);
@@ -1136,14 +1138,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   sh.alpha = reinterpret_cast<float*>(base + L::kAlphaOff);
   sh.fin = reinterpret_cast<float*>(base + L::kFinOff);
   sh.rowoff = reinterpret_cast<int32_t*>(base + L::kRowOff);
-  sh.res = smem_u32(base + L::kResOff);
+  sh.res = s0 + L::kResOff;
   sh.resp = reinterpret_cast<int32_t*>(base + L::kResOff);
-  sh.bars = smem_u32(base + L::kBarOff);
+  sh.bars = s0 + L::kBarOff;
   sh.tmem_slot = reinterpret_cast<uint32_t*>(base + L::kMiscOff);
   sh.abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
   sh.rescale_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 8);
   sh.overflow = reinterpret_cast<volatile int*>(base + L::kMiscOff + 16);
-  sh.ones = smem_u32(base + L::kOnesOff);
+  sh.ones = s0 + L::kOnesOff;
 
   const int warp = threadIdx.x >> 5;
   long long lo = 0;

@@ -115,39 +115,40 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(smem desc) * B(smem desc), bf16 inputs, fp32 accumulate, one CTA. Executed by
-// a whole warp: only the lane with `issue` set issues the MMA (a predicated instruction, so the
-// warp never diverges around the issue stream).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate, bool issue = true) {
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
-      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(issue))
-      : "memory");
-}
-// Arrive once on the mbarrier when every previously issued MMA of this thread has completed
-// (issued by the lane with `issue` set).
-__device__ __forceinline__ void mma_commit(uint32_t bar, bool issue = true) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
-      " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar),
-      "r"(static_cast<uint32_t>(issue))
-      : "memory");
-}
-
-// Warp-collective forms of the two above: every lane of the converged warp executes them and
+// D(tmem) (+)= A(smem desc) * B(smem desc), bf16 inputs, fp32 accumulate, one CTA: four MMAs
+// along K in one warp-collective block. Every lane of the converged warp executes it and
 // elect.sync picks the issuing lane (the same lane for every call of a converged warp, so a
-// commit tracks the MMAs issued before it). Measured on GB300 with a 76-MMA tile sequence
-// (M = 128, N = 64): ~52 cycles per MMA, against ~68 with a lane-0 predicate.
-__device__ __forceinline__ void mma_bf16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
+// commit tracks the MMAs issued before it); the MMAs are predicated, so the warp never
+// diverges around the issue stream. A descriptor is passed as its two 32-bit words: the low
+// word carries the start address (and the leading byte offset), the high word is constant per
+// operand layout; step k adds k * SA (k * SB) to the low word, i.e. 16 * SA bytes to A's start
+// address. Only the first MMA takes `accumulate`; the other three accumulate.
+//
+// Keeping the address arithmetic in 32 bits, with the per-step offsets as immediates and one
+// elect per group, shrinks an MMA from ~450 to ~125 bytes of code (the attention kernel
+// issues 112 of them per tile in straight-line code; with 64-bit descriptor adds it was
+// dominated by them).
+template <int SA, int SB>
+__device__ __forceinline__ void mma_bf16_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p, q;\n .reg .b32 r;\n elect.sync r|q, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
-      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n .reg .pred p, q;\n .reg .b32 r, a1, b1;\n .reg .b64 da, db;\n"
+      " elect.sync r|q, 0xffffffff;\n setp.ne.b32 p, %6, 0;\n"
+      " mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+      " setp.eq.b32 p, 0, 0;\n"
+      " add.u32 a1, %1, %7;\n add.u32 b1, %3, %8;\n mov.b64 da, {a1, %2};\n mov.b64 db, {b1, %4};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+      " add.u32 a1, %1, %9;\n add.u32 b1, %3, %10;\n mov.b64 da, {a1, %2};\n mov.b64 db, {b1, %4};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n"
+      " add.u32 a1, %1, %11;\n add.u32 b1, %3, %12;\n mov.b64 da, {a1, %2};\n mov.b64 db, {b1, %4};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(SA), "n"(SB), "n"(2 * SA),
+      "n"(2 * SB), "n"(3 * SA), "n"(3 * SB)
       : "memory");
 }
+// Arrive once on the mbarrier when every MMA previously issued by the warp's elected lane has
+// completed (warp-collective, like the MMAs).
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n .reg .pred q;\n .reg .b32 r;\n elect.sync r|q, 0xffffffff;\n"
@@ -227,18 +228,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ UMMA descriptors
-// Shared-memory matrix descriptor (tcgen05): start address, leading- and stride-dimension
-// byte offsets (all >> 4), descriptor version 1 at bits 46-47, swizzle mode at bits 61-63.
+// Shared-memory matrix descriptor (tcgen05), as two 32-bit words. Low word: start address >> 4
+// (bits 0-13) and leading-dimension byte offset >> 4 (bits 16-29). High word: stride-dimension
+// byte offset >> 4 (bits 32-45 of the descriptor), descriptor version 1 (bit 46), swizzle mode
+// (bits 61-63). A shared address is below 2^18, so adding a byte offset >> 4 that stays inside
+// the shared window to the low word never carries out of the start-address field.
 enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle32B = 6 };
 
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(swz) << 61;
-  return d;
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo, uint32_t swz) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (swz << 29);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.

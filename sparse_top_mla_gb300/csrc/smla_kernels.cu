@@ -49,9 +49,11 @@ __device__ int g_device_error;
 
 // Event timestamps (global timer, ns) per CTA for timeline analysis; compiled in only with
 // -DSMLA_TRACE. Slot layout: 0 entry, 1 after the dependency wait, 2 exit, 3 first rows
-// published, 4 first loads issued; tile j < 24 at 8 + 10j: +0 S^T ready, +1 fast pass done,
-// +2 P^T final (issuer), +3 PV issued, +4 blocks 0-3 stored (issuer), +5 blocks 4-8 stored
-// (issuer), +6/+7 the loaders' arrivals, +8/+9 epilogue start/end.
+// published, 4 first loads issued; tile j < 10 at 8 + 24j: +0 S^T ready, +1 fast pass done,
+// +2 P^T final (issuer), +3 PV issued, +4 / +10 / +5 blocks 0-3 / 4-7 / 8 stored (issuer),
+// +6 / +7 / +11 the loaders' arrivals for them, +8/+9 epilogue start/end, +12..15 the loaders
+// past the release of block pair 0..3, +16..19 block pair 0..3 stored, +20..23 its refill
+// issued.
 #ifdef SMLA_TRACE
 __device__ unsigned long long g_trace[1024][256];
 #define SMLA_TRACE_AT(slot)                                                  \
@@ -60,7 +62,7 @@ __device__ unsigned long long g_trace[1024][256];
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                  \
     if (blockIdx.x < 1024 && (slot) < 256) g_trace[blockIdx.x][(slot)] = t_; \
   } while (0)
-#define SMLA_TRACE_TILE(j, k) SMLA_TRACE_AT(((j) < 24 ? 8 + 10 * (j) + (k) : 255))
+#define SMLA_TRACE_TILE(j, k) SMLA_TRACE_AT(((j) < 10 ? 8 + 24 * (j) + (k) : 255))
 #else
 #define SMLA_TRACE_AT(slot) \
   do {                      \
@@ -102,8 +104,7 @@ struct Smem {
   static constexpr int kBarOff = kResOff + 2 * 5 * kTile * 4;   // mbarriers
   static constexpr int kNumBars = 24;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;       // tmem base, flags
-  static constexpr int kOnesOff = kMiscOff + 128;               // 128 B of bf16 1.0 (row-sum operand)
-  static constexpr int kBytes = kOnesOff + 128;
+  static constexpr int kBytes = kMiscOff + 128;
   static constexpr int kAlloc = kBytes + 1024;                  // + alignment slack
 };
 static_assert(Smem<64>::kAlloc <= 232448, "shared memory budget");
@@ -125,6 +126,12 @@ struct TmemCols {
   static constexpr int kL = 64;   // row sums of P per head, accumulated by the tensor core (all lanes equal)
   static constexpr int kO = 128;  // O^T block b at kO + b*NH
   static constexpr int kAlloc = (kO + 4 * NH) <= 256 ? 256 : 512;
+  // bf16 1.0 in 16 columns, the A operand of the row sums (read from TMEM, so the row sums
+  // take no shared-memory bandwidth for it): past O^T, or in the gap after S^T when O^T fills
+  // the allocation
+  static constexpr int kOnes = (kO + 4 * NH + 16) <= kAlloc ? kO + 4 * NH : 32;
+  static_assert((kOnes >= kO + 4 * NH && kOnes + 16 <= kAlloc) || (kOnes >= NH && kOnes + 16 <= kL),
+                "ones columns overlap another TMEM region");
 };
 
 struct Shared {
@@ -139,7 +146,6 @@ struct Shared {
   volatile int* abort_flag;
   volatile int* rescale_flag;
   volatile int* overflow;  // [2] tag j+1: a score of tile j passed its threshold (by tile parity)
-  uint32_t ones;           // 128 B of bf16 1.0
   __device__ uint32_t bar(int i) const { return bars + 8u * i; }
 };
 
@@ -600,12 +606,14 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
     auto step = [&](auto bpc) -> bool {
       constexpr int bp = decltype(bpc)::value;
       if (j > 0 && !wait_bar_w(sh, sh.bar(kBarPvDone + bp), (j - 1) & 1)) return false;
+      if (u == 0) SMLA_TRACE_TILE(j, 12 + bp);
       if (bp == 0 && first && j > 0) load_q(cur.item);
       if (fmt_cur == 1) {
         ld_store_fp8<bp>(sh, rg, lane8, bp, D, dq);
       } else {
         ld_store_bf16<(bp & 1)>(sh, rg, lane8, bp, D);
       }
+      if (u == 0) SMLA_TRACE_TILE(j, 16 + bp);
       if (bp == 0 && first) cp_async_wait_all();
       if (bp & 1) {  // blocks 0-3 (after bp 1) or 4-7 (after bp 3) complete
         fence_proxy_async_smem();
@@ -622,6 +630,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(sh.bar(kBarFullR));
+        if (u == 0) SMLA_TRACE_TILE(j, 11);
       }
       // first tile: an fp8 tile's first refill already needs the next rows; a bf16 tile's
       // first refills still read the current tile
@@ -652,6 +661,7 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
           if (bp == 3) ld_issue_rope(1, cache_nxt, off_nxt, lane8, D);
         }
       }
+      if (u == 0) SMLA_TRACE_TILE(j, 20 + bp);
       if (j == 0 && bp == 0 && has1 && fmt_cur != 1 && !next_rows()) return false;
       if (fmt_cur == 1 && bp < 3) ld_dequant_fp8<(bp < 3 ? bp + 1 : 3)>(D, dq);
       return true;
@@ -669,11 +679,10 @@ __device__ __forceinline__ void loader_role(const AttnArgs& a, const Shared& sh,
 // Descriptor low words are built once per call; each MMA adds a compile-time byte offset (>> 4)
 // to the start address field. The high words are constants of the operand layouts.
 struct MmaDesc {
-  uint32_t qk_a, qk_b, pv_a, pv_b, ones;
+  uint32_t qk_a, qk_b, pv_a, pv_b;
 };
 constexpr uint32_t kHiK128 = smem_desc_hi(1024, kSwizzle128B);  // K-major, 128B swizzle, 8-row groups 1 KB apart
 constexpr uint32_t kHiP = smem_desc_hi(2048, kSwizzleNone);     // P^T: 8x8 core matrices, N groups 2 KB apart
-constexpr uint32_t kHiOnes = smem_desc_hi(0, kSwizzleNone);     // the ones operand: every group the same 128 B
 
 template <int NH>
 __device__ __forceinline__ MmaDesc make_descs(const Shared& sh) {
@@ -682,7 +691,6 @@ __device__ __forceinline__ MmaDesc make_descs(const Shared& sh) {
   d.qk_b = smem_desc_lo(sh.q, 16);
   d.pv_a = smem_desc_lo(sh.tile, kBlockBytes);
   d.pv_b = smem_desc_lo(sh.tile + 8 * kBlockBytes, 128);
-  d.ones = smem_desc_lo(sh.ones, 0);  // every row and K step reads the same ones
   return d;
 }
 
@@ -701,7 +709,7 @@ __device__ __forceinline__ bool mma_qk(const Shared& sh, const MmaDesc& d, uint3
     if (kb == 0 || kb == 4 || kb == 8) {
       if (!wait_bar_w(sh, sh.bar(kb == 0 ? kBarFullA : (kb == 4 ? kBarFullB : kBarFullR)), j & 1)) return false;
       tc_fence_after();
-      if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, kb == 0 ? 4 : 5);
+      if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, kb == 0 ? 4 : (kb == 4 ? 10 : 5));
     }
     // four K steps of 16 channels: 32 bytes along the swizzled row of block kb
     mma_bf16_x4<2, 2>(tmem + TmemCols<NH>::kS, d.qk_a + static_cast<uint32_t>((kb * kBlockBytes) >> 4), kHiK128,
@@ -728,8 +736,9 @@ __device__ __forceinline__ void mma_pv(const Shared& sh, const MmaDesc& d, uint3
 template <int NH>
 __device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool first) {
   constexpr uint32_t idesc = idesc_bf16(128, NH, 0, 1);
-  mma_bf16_x4<0, 16>(tmem + TmemCols<NH>::kL, d.ones, kHiOnes, d.pv_b, kHiP, idesc, first ? 0u : 1u);
-  mma_bf16_x4<0, 16>(tmem + TmemCols<NH>::kL, d.ones, kHiOnes, d.pv_b + 64, kHiP, idesc, 1u);
+  const uint32_t ones = tmem + TmemCols<NH>::kOnes;
+  mma_bf16_ts_x4<16>(tmem + TmemCols<NH>::kL, ones, d.pv_b, kHiP, idesc, first ? 0u : 1u);
+  mma_bf16_ts_x4<16>(tmem + TmemCols<NH>::kL, ones, d.pv_b + 64, kHiP, idesc, 1u);
 }
 
 // QK^T of the first tile of the stream.
@@ -872,6 +881,16 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   (void)tr_first;
   int nfix = 0;  // rescale passes so far (phase of PFixed)
   if (n <= 0) return;
+  {
+    // the row sums' A operand (bf16 1.0 pairs) in this warp's TMEM lanes; the issuer first reads
+    // it after the PFixed barrier of the stream's first tile, which every warp reaches with a
+    // fence after this store
+    float ones[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ones[i] = __uint_as_float(0x3F803F80u);
+    tmem_st16(tl + TC::kOnes, ones);
+    tmem_st_wait();
+  }
 
   // ---- index resolution, by warps 0-2 (warp 0 also takes rows 96-127, so the issuing warp
   // stays free)
@@ -1145,7 +1164,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   sh.abort_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 4);
   sh.rescale_flag = reinterpret_cast<volatile int*>(base + L::kMiscOff + 8);
   sh.overflow = reinterpret_cast<volatile int*>(base + L::kMiscOff + 16);
-  sh.ones = s0 + L::kOnesOff;
 
   const int warp = threadIdx.x >> 5;
   long long lo = 0;
@@ -1173,7 +1191,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
     sh.overflow[0] = sh.overflow[1] = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 32) reinterpret_cast<uint32_t*>(base + L::kOnesOff)[threadIdx.x] = 0x3F803F80u;
   fence_proxy_async_smem();
   if (warp == 0) {
     tmem_alloc(smem_u32(sh.tmem_slot), TmemCols<NH>::kAlloc);

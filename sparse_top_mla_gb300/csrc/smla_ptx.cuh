@@ -147,6 +147,27 @@ __device__ __forceinline__ void mma_bf16_x4(uint32_t d_tmem, uint32_t a_lo, uint
       "n"(2 * SB), "n"(3 * SA), "n"(3 * SB)
       : "memory");
 }
+// The same with A read from TMEM (tcgen05 "A in tensor memory" form): a_tmem is the TMEM
+// address of A's 128 lanes x 16 bf16 (8 columns); every K step reads the same A, and B advances
+// by SB per step.
+template <int SB>
+__device__ __forceinline__ void mma_bf16_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n .reg .b32 r, b1;\n .reg .b64 db;\n"
+      " elect.sync r|q, 0xffffffff;\n setp.ne.b32 p, %5, 0;\n"
+      " mov.b64 db, {%2, %3};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
+      " setp.eq.b32 p, 0, 0;\n"
+      " add.u32 b1, %2, %6;\n mov.b64 db, {b1, %3};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
+      " add.u32 b1, %2, %7;\n mov.b64 db, {b1, %3};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n"
+      " add.u32 b1, %2, %8;\n mov.b64 db, {b1, %3};\n"
+      " @q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(SB), "n"(2 * SB), "n"(3 * SB)
+      : "memory");
+}
 // Arrive once on the mbarrier when every MMA previously issued by the warp's elected lane has
 // completed (warp-collective, like the MMAs).
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {

@@ -365,6 +365,25 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizz
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// TMEM columns [c, c+W) of this warp's lanes into v (W = 16 or 32): issue, and the wait that
+// makes v usable (it waits for every earlier load of the thread).
+template <int W>
+__device__ __forceinline__ void tmem_load_nw(uint32_t addr, float* v) {
+  if constexpr (W == 32) {
+    tmem_ld32_nw(addr, v);
+  } else {
+    tmem_ld16_nw(addr, v);
+  }
+}
+template <int W>
+__device__ __forceinline__ void tmem_load_wait(float* v) {
+  if constexpr (W == 32) {
+    tmem_ld_wait32(v);
+  } else {
+    tmem_ld_wait16(v);
+  }
+}
+
 // TMEM columns [c, c+W) of this warp's lanes into v (W = 16 or 32), waited.
 template <int W>
 __device__ __forceinline__ void tmem_load(uint32_t addr, float* v) {
@@ -741,21 +760,23 @@ __device__ __forceinline__ void mma_rowsum(const MmaDesc& d, uint32_t tmem, bool
   mma_bf16_ts_x4<16>(tmem + TmemCols<NH>::kL, ones, d.pv_b + 64, kHiP, idesc, 1u);
 }
 
-// QK^T of the first tile of the stream.
+// QK^T of tile j as its blocks arrive, then the commit that tells the softmax warps S^T is ready.
 template <int NH>
-__device__ __forceinline__ bool mma_issue_first(const Shared& sh, uint32_t tmem) {
+__device__ __forceinline__ bool mma_issue_qk(const Shared& sh, uint32_t tmem, int j) {
   const MmaDesc d = make_descs<NH>(sh);
-  if (!mma_qk<NH>(sh, d, tmem, 0)) return false;
+  if (!mma_qk<NH>(sh, d, tmem, j)) return false;
   mma_commit_warp(sh.bar(kBarSFull));
   return true;
 }
 
 // After the softmax of tile j: PV of all four block pairs (each with its own commit, so the
 // loaders refill a block pair as soon as it is released), then the row sums with their own
-// commit (the loaders store the next rope block, where this tile's P^T lives, after it), then
-// QK^T of tile j+1 as its blocks arrive.
+// commit (the loaders store the next rope block, where this tile's P^T lives, after it). QK^T of
+// tile j+1 follows at the top of the next iteration of the tile loop; when tile j ends an item
+// the issuing warp first writes its share of the outputs (waiting for tile j+1's blocks first
+// would hold back the next softmax, which needs every warp).
 template <int NH>
-__device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem, int j, int n, bool first) {
+__device__ __forceinline__ void mma_issue_pv(const Shared& sh, uint32_t tmem, int j, bool first) {
   const MmaDesc d = make_descs<NH>(sh);
   tc_fence_after();
 #pragma unroll 1
@@ -763,10 +784,6 @@ __device__ __forceinline__ bool mma_issue_after(const Shared& sh, uint32_t tmem,
   mma_rowsum<NH>(d, tmem, first);
   mma_commit_warp(sh.bar(kBarRowsum));
   if (threadIdx.x == kIssueWarp * 32) SMLA_TRACE_TILE(j, 3);
-  if (j + 1 >= n) return true;
-  if (!mma_qk<NH>(sh, d, tmem, j + 1)) return false;
-  mma_commit_warp(sh.bar(kBarSFull));
-  return true;
 }
 
 // ------------------------------------------------------------------ softmax / epilogue role
@@ -927,13 +944,16 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
   }
   if (tid == 0) SMLA_TRACE_AT(3);
 
-  if (warp == kIssueWarp && !mma_issue_first<NH>(sh, tmem)) return;
 
   Cursor cur;
   cur.init(a, lo);
   for (int j = 0; j < n; ++j, cur.next(a)) {
     const bool first = cur.tile == 0 || j == 0;
     const bool last = cur.tile == a.tiles_per_item - 1 || j == n - 1;
+    if (warp == kIssueWarp) {
+      tc_fence_after();
+      if (!mma_issue_qk<NH>(sh, tmem, j)) return;
+    }
     // resolution runs while QK^T of tile j is in flight, so tile j+3's rows are published before
     // the loaders look for them at the start of their next tile. It reuses the row slot of tile
     // j-1, whose readers (the loaders, two and three tiles earlier) finished before that tile's
@@ -970,15 +990,16 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       if (fix && !wait_bar_w(sh, sh.bar(kBarPFixed), nfix & 1)) return;
       if (lane == 0) SMLA_TRACE_TILE(j, 2);
       tc_fence_after();
-      if (!mma_issue_after<NH>(sh, tmem, j, n, first)) return;
+      mma_issue_pv<NH>(sh, tmem, j, first);
     }
     if (fix) ++nfix;
 
     if (!last) continue;
     // ---- epilogue of the item segment: wait for its last PV (and row sums). Every TMEM lane of
     // L holds the same row sums, so each warp derives the output factors of the heads it writes
-    // from its own lanes: no step across warps (the issuing warp may still be queueing the next
-    // tile's QK^T while the other warps write). Warp 0 also writes the LSEs.
+    // from its own lanes: no step across warps (each warp moves on to the next tile as soon as
+    // its own share is written; the issuing warp then issues the next tile's QK^T). Warp 0 also
+    // writes the LSEs.
     if (!wait_bar_w(sh, sh.bar(kBarRowsum), j & 1)) return;
     tc_fence_after();
     if (tid == 0) SMLA_TRACE_TILE(j, 8);
@@ -997,6 +1018,12 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
       // out head c0+i's factor (and warp 0 its LSE) into this warp's row of the reduction
       // area, which the max pass does not use until every warp has left its epilogue.
       float* fw = sh.red + warp * 64;
+      // O^T blocks 0..3 of these heads: block 0's load is in flight while the factors are worked
+      // out; for NH <= 32 two register buffers also keep each later block's load in flight while
+      // the previous one is converted and stored
+      float oa[CW], ob[CW];
+      (void)ob;
+      tmem_load_nw<CW>(tl + TC::kO + c0, oa);
       {
         float l[CW];
         tmem_load<CW>(tl + TC::kL + c0, l);
@@ -1031,17 +1058,37 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
         f[i + 3] = v.w;
       }
       if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(249);
+      auto emit_blocks = [&](auto&& emit) {
+        if constexpr (NH <= 32) {
+#pragma unroll 1
+          for (int b = 0; b < 4; b += 2) {
+            tmem_load_wait<CW>(oa);
+            if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
+            tmem_load_nw<CW>(tl + TC::kO + (b + 1) * NH + c0, ob);
+            emit(oa, b);
+            tmem_load_wait<CW>(ob);
+            if (b + 2 < 4) tmem_load_nw<CW>(tl + TC::kO + (b + 2) * NH + c0, oa);
+            emit(ob, b + 1);
+          }
+        } else {
+          // one buffer: the second copy of the conversion code costs the larger kernels more in
+          // instruction fetch than the overlap gains
+#pragma unroll 1
+          for (int b = 0; b < 4; ++b) {
+            if (b > 0) tmem_load_nw<CW>(tl + TC::kO + b * NH + c0, oa);
+            tmem_load_wait<CW>(oa);
+            if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
+            emit(oa, b);
+          }
+        }
+      };
       if (a.split) {
         // partial O^T in head chunks of 8: entry (channel, 8 heads) of chunk k is 16 bytes at
         // ((slot*T + t)*nchunks + k)*512 + channel, so a warp's 32 channels are 512 contiguous
         // bytes per store
         uint4* pbase = reinterpret_cast<uint4*>(a.part_o) +
                        ((static_cast<int64_t>(slot) * a.T + t) * a.nchunks + ((h0 + c0) >> 3)) * kDv + tid;
-#pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-          float o[CW];
-          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
-          if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
+        auto emit = [&](const float* o, int b) {
 #pragma unroll
           for (int g8 = 0; g8 < CW / 8; ++g8) {
             if (c0 + 8 * g8 < hg) {
@@ -1057,7 +1104,8 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
             }
           }
           if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(251 + (b < 2 ? b : (b == 3 ? 2 : 5)));
-        }
+        };
+        emit_blocks(emit);
       } else {
         // final O: thread tid holds channel 128b + tid of every head. Within each group of 8
         // lanes an 8x8 transpose of the bf16 values (three exchange stages on pairs packed two
@@ -1067,11 +1115,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
             a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
         const int64_t hstride = a.out_stride_h;
         const int k8 = lane & 7;
-#pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-          float o[CW];
-          tmem_load<CW>(tl + TC::kO + b * NH + c0, o);
-          if (tid == 0 && tr_first && c0 == 0 && b == 0) SMLA_TRACE_AT(250);
+        auto emit = [&](float* o, int b) {
 #pragma unroll
           for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
 #pragma unroll
@@ -1127,7 +1171,8 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
               *reinterpret_cast<uint4*>(obase + h * hstride + b * 128 + (tid & ~7)) = make_uint4(p[0], p[1], p[2], p[3]);
           }
           if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(251 + (b < 2 ? b : (b == 3 ? 2 : 5)));
-        }
+        };
+        emit_blocks(emit);
       }
       if (tid == 0 && tr_first) SMLA_TRACE_AT(254);
     }

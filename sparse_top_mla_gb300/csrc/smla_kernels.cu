@@ -1028,9 +1028,15 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
         float l[CW];
         tmem_load<CW>(tl + TC::kL + c0, l);
         if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(248);
-        float lsel = l[0];
+        // lane i takes column c0+i (every lane holds the same sums): a select tree on the lane's
+        // bits, log2(CW) levels
 #pragma unroll
-        for (int i = 1; i < CW; ++i) lsel = (i == lane) ? l[i] : lsel;
+        for (int w = CW / 2, bit = 0; w >= 1; w /= 2, ++bit) {
+          const bool hi = ((lane >> bit) & 1) != 0;
+#pragma unroll
+          for (int i = 0; i < w; ++i) l[i] = hi ? l[2 * i + 1] : l[2 * i];
+        }
+        const float lsel = l[0];
         if (lane < CW) {
           const int h = c0 + lane;
           const float m = sh.m_run[h];
@@ -1048,14 +1054,14 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
         }
         __syncwarp();
       }
-      float f[CW];
+      // factors of head pairs, packed for the paired fp32 multiply (an empty head's factor is 0
+      // and its O^T column is 0, so its outputs are 0)
+      uint64_t f2[CW / 2];
 #pragma unroll
       for (int i = 0; i < CW; i += 4) {
         const float4 v = *reinterpret_cast<const float4*>(fw + c0 + i);
-        f[i] = v.x;
-        f[i + 1] = v.y;
-        f[i + 2] = v.z;
-        f[i + 3] = v.w;
+        f2[i / 2] = pack_f32x2(v.x, v.y);
+        f2[i / 2 + 1] = pack_f32x2(v.z, v.w);
       }
       if (tid == 0 && tr_first && c0 == 0) SMLA_TRACE_AT(249);
       auto emit_blocks = [&](auto&& emit) {
@@ -1096,9 +1102,7 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = 8 * g8 + 2 * e;
-                const __nv_bfloat162 bb = __floats2bfloat162_rn(f[i] != 0.f ? o[i] * f[i] : 0.f,
-                                                                f[i + 1] != 0.f ? o[i + 1] * f[i + 1] : 0.f);
-                w4[e] = *reinterpret_cast<const uint32_t*>(&bb);
+                w4[e] = mul_pack_bf16x2(o[i], o[i + 1], f2[i / 2]);
               }
               pbase[static_cast<int64_t>(g8) * kDv + 128 * b] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
@@ -1115,18 +1119,13 @@ __device__ __forceinline__ void softmax_role(const AttnArgs& a, const Shared& sh
             a.out + static_cast<int64_t>(t) * a.out_stride_t + static_cast<int64_t>(h0) * a.out_stride_h;
         const int64_t hstride = a.out_stride_h;
         const int k8 = lane & 7;
-        auto emit = [&](float* o, int b) {
-#pragma unroll
-          for (int i = 0; i < CW; ++i) o[i] = f[i] != 0.f ? o[i] * f[i] : 0.f;
+        auto emit = [&](const float* o, int b) {
 #pragma unroll
           for (int q = 0; q < CW / 8; ++q) {
             // heads c0+8q .. c0+8q+7 of this lane's channel, as bf16 pairs (p[m] = heads 2m, 2m+1)
             uint32_t p[4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const __nv_bfloat162 bb = __floats2bfloat162_rn(o[8 * q + 2 * m], o[8 * q + 2 * m + 1]);
-              p[m] = *reinterpret_cast<const uint32_t*>(&bb);
-            }
+            for (int m = 0; m < 4; ++m) p[m] = mul_pack_bf16x2(o[8 * q + 2 * m], o[8 * q + 2 * m + 1], f2[4 * q + m]);
             // 8x8 transpose of bf16 elements across the 8 lanes of the group, in three exchange
             // stages: lane pairs k, k^4 swap whole words 2,3 <-> 0,1; k, k^2 swap words 1,3 <->
             // 0,2; k, k^1 swap the odd <-> even halves of every word (packed two to a word)

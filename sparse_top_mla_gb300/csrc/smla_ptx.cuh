@@ -276,6 +276,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 }
 
 // ------------------------------------------------------------------ math helpers
+__device__ __forceinline__ uint64_t pack_f32x2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+// bf16x2 of (a * f.lo, b * f.hi): one paired fp32 multiply (round to nearest), one rounding to
+// bf16 (RNE); a's result in the low half.
+__device__ __forceinline__ uint32_t mul_pack_bf16x2(float a, float b, uint64_t f) {
+  uint32_t out;
+  asm("{\n .reg .b64 x;\n .reg .f32 lo, hi;\n mov.b64 x, {%1, %2};\n mul.rn.f32x2 x, x, %3;\n"
+      " mov.b64 {lo, hi}, x;\n cvt.rn.bf16x2.f32 %0, hi, lo;\n}\n"
+      : "=r"(out)
+      : "f"(a), "f"(b), "l"(f));
+  return out;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -84,33 +84,53 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __g
   const int lane = threadIdx.x & 31;
   const long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
   if (i >= q.n) return;
-  const long long slot = q.slots[i];
-  if (slot < 0 || slot >= q.num_slots) return;
   const uint8_t* in = q.kv + i * q.kv_stride_bytes;
-  uint8_t* out = q.cache + (slot >> 6) * q.page_stride + (slot & 63) * q.row_stride;
 
   if (!q.fp8) {
-    // bf16 row: 576 channels = 72 chunks of 8 values
-    for (int ch = lane; ch < 72; ch += 32) {
-      uint4 o;
-      if (q.in_f32) {
-        const uint4 a = ldg_v4(in + 32 * ch);
-        const uint4 b = ldg_v4(in + 32 * ch + 16);
-        o = make_uint4(bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
-                       bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
-                       bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
-                       bf16x2(__uint_as_float(b.z), __uint_as_float(b.w)));
-      } else {
-        o = ldg_v4(in + 16 * ch);
+    // bf16 row: 576 channels = 72 chunks of 8 values; every load is issued before the slot is
+    // known (they do not depend on it)
+    uint4 o[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const int ch = lane + 32 * r;
+      o[r] = make_uint4(0, 0, 0, 0);
+      if (ch < 72) {
+        if (q.in_f32) {
+          const uint4 a = ldg_v4(in + 32 * ch);
+          const uint4 b = ldg_v4(in + 32 * ch + 16);
+          o[r] = make_uint4(bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
+                            bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
+                            bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
+                            bf16x2(__uint_as_float(b.z), __uint_as_float(b.w)));
+        } else {
+          o[r] = ldg_v4(in + 16 * ch);
+        }
       }
-      *reinterpret_cast<uint4*>(out + 16 * ch) = o;
     }
+    const long long slot = q.slots[i];
+    if (slot < 0 || slot >= q.num_slots) return;
+    uint8_t* out = q.cache + (slot >> 6) * q.page_stride + (slot & 63) * q.row_stride;
+#pragma unroll
+    for (int r = 0; r < 3; ++r)
+      if (lane + 32 * r < 72) *reinterpret_cast<uint4*>(out + 16 * (lane + 32 * r)) = o[r];
     return;
   }
 
-  // FP8 row: latent channels 16*lane .. 16*lane+15 belong to block lane/8
+  // FP8 row: latent channels 16*lane .. 16*lane+15 belong to block lane/8; the latent, rope and
+  // slot loads are all issued before any of them is used
   float x[16];
   load16(q, in, 16 * lane, x);
+  uint4 ra = make_uint4(0, 0, 0, 0), rb = make_uint4(0, 0, 0, 0);
+  if (lane < 8) {
+    if (q.in_f32) {
+      const uint8_t* r = in + 4 * (kDv + 8 * lane);
+      ra = ldg_v4(r);
+      rb = ldg_v4(r + 16);
+    } else {
+      ra = ldg_v4(in + 2 * (kDv + 8 * lane));
+    }
+  }
+  const long long slot = q.slots[i];
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
@@ -125,28 +145,23 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __g
     const uint32_t hi = e4m3x2(__fdiv_rn(x[4 * k + 2], scale), __fdiv_rn(x[4 * k + 3], scale));
     w[k] = lo | (hi << 16);
   }
-  *reinterpret_cast<uint4*>(out + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
-  // the four block scales, gathered into lane 0 and stored as one 16-byte write
+  // the four block scales, gathered into lane 0
   const float s1 = __shfl_sync(0xffffffffu, scale, 8);
   const float s2 = __shfl_sync(0xffffffffu, scale, 16);
   const float s3 = __shfl_sync(0xffffffffu, scale, 24);
+  if (slot < 0 || slot >= q.num_slots) return;
+  uint8_t* out = q.cache + (slot >> 6) * q.page_stride + (slot & 63) * q.row_stride;
+  *reinterpret_cast<uint4*>(out + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
   if (lane == 0)
     *reinterpret_cast<uint4*>(out + kDv) =
         make_uint4(__float_as_uint(scale), __float_as_uint(s1), __float_as_uint(s2), __float_as_uint(s3));
   // rope: 64 channels -> bf16, 8 lanes x 8 channels
   if (lane < 8) {
-    uint4 o;
-    if (q.in_f32) {
-      const uint8_t* r = in + 4 * (kDv + 8 * lane);
-      const uint4 a = ldg_v4(r);
-      const uint4 b = ldg_v4(r + 16);
-      o = make_uint4(bf16x2(__uint_as_float(a.x), __uint_as_float(a.y)),
-                     bf16x2(__uint_as_float(a.z), __uint_as_float(a.w)),
-                     bf16x2(__uint_as_float(b.x), __uint_as_float(b.y)),
-                     bf16x2(__uint_as_float(b.z), __uint_as_float(b.w)));
-    } else {
-      o = ldg_v4(in + 2 * (kDv + 8 * lane));
-    }
+    const uint4 o = q.in_f32 ? make_uint4(bf16x2(__uint_as_float(ra.x), __uint_as_float(ra.y)),
+                                          bf16x2(__uint_as_float(ra.z), __uint_as_float(ra.w)),
+                                          bf16x2(__uint_as_float(rb.x), __uint_as_float(rb.y)),
+                                          bf16x2(__uint_as_float(rb.z), __uint_as_float(rb.w)))
+                             : ra;
     *reinterpret_cast<uint4*>(out + kDv + 16 + 16 * lane) = o;
   }
 }

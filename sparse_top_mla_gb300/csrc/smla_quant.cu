@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "smla.h"
@@ -80,10 +82,7 @@ __device__ __forceinline__ void load16(const QuantArgs& q, const uint8_t* row, i
   }
 }
 
-__global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __grid_constant__ QuantArgs q) {
-  const int lane = threadIdx.x & 31;
-  const long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-  if (i >= q.n) return;
+__device__ __forceinline__ void quantize_row(const QuantArgs& q, long long i, int lane) {
   const uint8_t* in = q.kv + i * q.kv_stride_bytes;
 
   if (!q.fp8) {
@@ -166,6 +165,37 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __g
   }
 }
 
+// Persistent: as many CTAs as fit on every SM at once, each warp walking the rows with the
+// grid's warp count as stride (short one-row CTAs left a third of the warp slots empty).
+__global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __grid_constant__ QuantArgs q) {
+  const int lane = threadIdx.x & 31;
+  const long long stride = static_cast<long long>(gridDim.x) * kQuantWarps;
+#pragma unroll 1
+  for (long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5); i < q.n; i += stride)
+    quantize_row(q, i, lane);
+}
+
+// Resident CTAs of quantize_kv_kernel on the current device (SMs x CTAs per SM), cached per
+// device.
+int quant_resident_ctas() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kv_kernel, kQuantWarps * 32, 0) !=
+          cudaSuccess ||
+      per_sm <= 0)
+    per_sm = 1;
+  const int n = sms * per_sm;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 }  // namespace
 }  // namespace smla
 
@@ -199,7 +229,8 @@ extern "C" smla_status smla_quantize_kv(const void* kv, int32_t kv_dtype, int64_
   q.page_stride = page_stride_bytes;
   q.num_slots = static_cast<int64_t>(num_pages) * kPage;
   q.fp8 = format == SMLA_KV_FP8_E4M3_S128 ? 1 : 0;
-  const unsigned grid = static_cast<unsigned>((static_cast<long long>(n) + kQuantWarps - 1) / kQuantWarps);
+  const long long want = (static_cast<long long>(n) + kQuantWarps - 1) / kQuantWarps;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(want, quant_resident_ctas()));
   quantize_kv_kernel<<<grid, kQuantWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(q);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

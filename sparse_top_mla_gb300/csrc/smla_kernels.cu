@@ -299,39 +299,19 @@ __device__ __forceinline__ void publish_done(const Shared& sh, int jt, int lane)
 }
 
 // ------------------------------------------------------------------ helpers
-template <int CNT, int OFF, bool kMax>
-__device__ __forceinline__ void col_reduce_step(float* v, int lane) {
-  if constexpr (OFF > 0) {
-    if constexpr (CNT > 1) {
-      constexpr int half = CNT / 2;
-      const bool upper = (lane & OFF) != 0;
+// Column maxima of N (16 or 32) values per lane across the warp: one warp-wide float max
+// reduction (`redux.sync.max.f32`, every lane receives the result) per column; lane c keeps
+// column c's and writes it to red_w[c].
+template <int N>
+__device__ __forceinline__ void warp_col_max_store(const float* v, int lane, float* red_w) {
+  float mine = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < half; ++k) {
-        const float send = upper ? v[k] : v[k + half];
-        const float keep = upper ? v[k + half] : v[k];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, OFF);
-        v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
-      }
-      col_reduce_step<half, OFF / 2, kMax>(v, lane);
-    } else {
-      const float recv = __shfl_xor_sync(0xffffffffu, v[0], OFF);
-      v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
-      col_reduce_step<1, OFF / 2, kMax>(v, lane);
-    }
+  for (int c = 0; c < N; ++c) {
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v[c]));
+    mine = lane == c ? r : mine;
   }
-}
-
-// Column reduction of N (16 or 32) values per lane across the warp ("transpose reduce":
-// each step halves the values a lane holds and exchanges the other half with its partner,
-// N-1 shuffles in total). Writes the warp's column results to red_w[0..N).
-template <int N, bool kMax>
-__device__ __forceinline__ void warp_col_reduce_store(float* v, int lane, float* red_w) {
-  col_reduce_step<N, 16, kMax>(v, lane);
-  if (N == 32) {
-    red_w[lane] = v[0];
-  } else if ((lane & 1) == 0) {
-    red_w[lane >> 1] = v[0];
-  }
+  if (lane < N) red_w[lane] = mine;
 }
 
 // One e4m3 pair -> bf16x2: exact conversion to f16x2 and then to two fp32 values, one packed
@@ -839,7 +819,7 @@ __device__ __forceinline__ bool max_pass(const AttnArgs& a, const Shared& sh, ui
     tmem_load<CW>(tmem_lane + TC::kS + c0, s);
 #pragma unroll
     for (int h = 0; h < CW; ++h) s[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
-    warp_col_reduce_store<CW, true>(s, lane, sh.red + warp * 64 + c0);
+    warp_col_max_store<CW>(s, lane, sh.red + warp * 64 + c0);
   }
   if (!sm_sync(sh, smph)) return false;
   if (warp == 0) {

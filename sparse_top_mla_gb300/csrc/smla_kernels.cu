@@ -1268,7 +1268,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   extern __shared__ float wts[];  // [max_slots][kCombineHeads]
   __shared__ float fac[kCombineHeads];
   __shared__ __align__(16) uint16_t ot[kCombineHeads][kCombineCh];
-  // launched as a programmatic dependent of the attention kernel: wait for its partials
+  // launched as a programmatic dependent of the attention kernel: wait for its partials. The
+  // next kernel on the stream may be scheduled at once (it waits for this grid's completion
+  // before its own first global access), so its set-up overlaps this grid's tail.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   const int hbase = blockIdx.y * kCombineHeads;

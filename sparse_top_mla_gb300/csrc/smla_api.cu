@@ -402,12 +402,14 @@ const char* smla_last_error(void) { return g_last_error; }
 
 smla_status smla_device_error(int32_t* code) {
   if (code == nullptr) return SMLA_ERR_INVALID;
-  int c = 0;
-  const cudaError_t e = read_and_clear_device_error(&c);
+  int c = 0, cq = 0;
+  cudaError_t e = read_and_clear_device_error(&c);
+  if (e == cudaSuccess) e = read_and_clear_quant_error(&cq);
   if (e != cudaSuccess) {
     note_cuda_error(e, "reading the device error word");
     return SMLA_ERR_CUDA;
   }
+  if (c == 0) c = cq;
   *code = c;
   return c == 0 ? SMLA_OK : SMLA_ERR_DEVICE;
 }

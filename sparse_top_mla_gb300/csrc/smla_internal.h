@@ -90,6 +90,8 @@ cudaError_t launch_attention(const AttnArgs& args, const Plan& plan, cudaStream_
                              cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 cudaError_t read_and_clear_device_error(int* code);
+// The cache writer's own device error word (its bounded waits), read and cleared.
+cudaError_t read_and_clear_quant_error(int* code);
 
 // Records a CUDA failure for smla_last_error (thread-local).
 void note_cuda_error(cudaError_t e, const char* where);

@@ -43,6 +43,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive on the mbarrier and raise its expected transaction bytes by `bytes` (the phase then
+// completes once that many bytes of asynchronous copies have landed).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) global -> this CTA's
+// shared memory, completing as transaction bytes on the mbarrier.
+__device__ __forceinline__ void cp_async_bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ cp.async (16 B, L2 only)
 // src_bytes = 16 copies, 0 zero-fills the destination without reading the source.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {

@@ -20,9 +20,16 @@
 
 #include "smla.h"
 #include "smla_internal.h"
+#include "smla_ptx.cuh"
 
 namespace smla {
 namespace {
+
+using namespace ptx;
+
+// Bounded waits of the cache writer (~2 s), reported through smla_device_error.
+__device__ int g_quant_error;
+constexpr long long kQuantSpinCycles = 4000000000LL;
 
 constexpr int kQuantWarps = 8;
 
@@ -82,9 +89,8 @@ __device__ __forceinline__ void load16(const QuantArgs& q, const uint8_t* row, i
   }
 }
 
-__device__ __forceinline__ void quantize_row(const QuantArgs& q, long long i, int lane) {
-  const uint8_t* in = q.kv + i * q.kv_stride_bytes;
-
+// One row from `in` (the row's 576 input values; shared memory here) to cache slot `slot`.
+__device__ __forceinline__ void quantize_row(const QuantArgs& q, const uint8_t* in, long long slot, int lane) {
   if (!q.fp8) {
     // bf16 row: 576 channels = 72 chunks of 8 values; every load is issued before the slot is
     // known (they do not depend on it)
@@ -106,7 +112,6 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& q, long long i, in
         }
       }
     }
-    const long long slot = q.slots[i];
     if (slot < 0 || slot >= q.num_slots) return;
     uint8_t* out = q.cache + (slot >> 6) * q.page_stride + (slot & 63) * q.row_stride;
 #pragma unroll
@@ -129,7 +134,6 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& q, long long i, in
       ra = ldg_v4(in + 2 * (kDv + 8 * lane));
     }
   }
-  const long long slot = q.slots[i];
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
@@ -166,13 +170,67 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& q, long long i, in
 }
 
 // Persistent: as many CTAs as fit on every SM at once, each warp walking the rows with the
-// grid's warp count as stride (short one-row CTAs left a third of the warp slots empty).
+// grid's warp count as stride. A warp keeps two rows in flight: lane 0 bulk-copies the next
+// row into the warp's other shared-memory buffer (completion on that buffer's mbarrier) while
+// the warp converts the current one; the slot word is also loaded a row ahead.
+__device__ __forceinline__ bool quant_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, 20000)) {
+    if (clock64() - t0 > kQuantSpinCycles) return false;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kv_kernel(const __grid_constant__ QuantArgs q) {
+  __shared__ __align__(128) uint8_t rows[kQuantWarps][2][kDqk * 4];
+  __shared__ __align__(8) uint64_t bars[kQuantWarps][2];
   const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const uint32_t bytes = q.in_f32 ? kDqk * 4 : kDqk * 2;
   const long long stride = static_cast<long long>(gridDim.x) * kQuantWarps;
+  long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + w;
+  const uint32_t bar0 = smem_u32(&bars[w][0]), bar1 = smem_u32(&bars[w][1]);
+  auto bar = [&](int b) { return b ? bar1 : bar0; };
+  if (lane == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar1, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (i >= q.n) return;
+  auto issue = [&](long long r, int b) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(b), bytes);
+      cp_async_bulk_g2s(smem_u32(rows[w][b]), q.kv + r * q.kv_stride_bytes, bytes, bar(b));
+    }
+  };
+  issue(i, 0);
+  long long slot = q.slots[i];
+  uint32_t phase = 0;  // bit b: parity of buffer b's next completion
 #pragma unroll 1
-  for (long long i = static_cast<long long>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5); i < q.n; i += stride)
-    quantize_row(q, i, lane);
+  for (int k = 0; i < q.n; ++k, i += stride) {
+    const int b = k & 1;
+    const long long nx = i + stride;
+    long long slot_nx = -1;
+    if (nx < q.n) {
+      // buffer b^1 was read in iteration k-1 (every lane finished before its __syncwarp): order
+      // those reads before the copy that refills it
+      fence_proxy_async_smem();
+      issue(nx, b ^ 1);
+      slot_nx = q.slots[nx];
+    }
+    if (!quant_wait(bar(b), (phase >> b) & 1u)) {
+      // a copy that never lands: report it, give the other buffer's copy a bounded wait, stop
+      if (lane == 0) atomicExch(&g_quant_error, 1);
+      if (nx < q.n) quant_wait(bar(b ^ 1), (phase >> (b ^ 1)) & 1u);
+      return;
+    }
+    phase ^= 1u << b;
+    quantize_row(q, rows[w][b], slot, lane);
+    __syncwarp();
+    slot = slot_nx;
+  }
 }
 
 // Resident CTAs of quantize_kv_kernel on the current device (SMs x CTAs per SM), cached per
@@ -197,6 +255,15 @@ int quant_resident_ctas() {
 }
 
 }  // namespace
+
+// Reads and clears the cache writer's device error word.
+cudaError_t read_and_clear_quant_error(int* code) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_quant_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(int));
+}
+
 }  // namespace smla
 
 using namespace smla;

@@ -141,11 +141,27 @@ __device__ __forceinline__ void quantize_row(const QuantArgs& q, const uint8_t* 
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
   const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  // x / scale rounded to nearest, sixteen times with one divisor: Markstein's correction of
+  // x * RN(1/scale) (P. Markstein, "Computation of elementary functions on the IBM RISC
+  // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b) and q = RN(a*y),
+  // the remainder a - b*q is exact in one fma and RN(q + (a - b*q)*y) = RN(a/b) whenever the
+  // quotient is a normal number. Quotients below the normal range all encode to E4M3 +-0,
+  // which the sign (kept by working on |x|) decides. A block scale below the normal range
+  // (amax < 448 * 2^-126) has no finite reciprocal: such blocks divide directly.
+  const bool direct = scale < 1.17549435e-38f;
+  const float ys = __frcp_rn(scale);
+  auto quot = [&](float v) {
+    if (direct) return __fdiv_rn(v, scale);
+    const float a = fabsf(v);
+    const float q0 = __fmul_rn(a, ys);
+    const float r = __fmaf_rn(-scale, q0, a);
+    return copysignf(__fmaf_rn(r, ys, q0), v);
+  };
   uint32_t w[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t lo = e4m3x2(__fdiv_rn(x[4 * k], scale), __fdiv_rn(x[4 * k + 1], scale));
-    const uint32_t hi = e4m3x2(__fdiv_rn(x[4 * k + 2], scale), __fdiv_rn(x[4 * k + 3], scale));
+    const uint32_t lo = e4m3x2(quot(x[4 * k]), quot(x[4 * k + 1]));
+    const uint32_t hi = e4m3x2(quot(x[4 * k + 2]), quot(x[4 * k + 3]));
     w[k] = lo | (hi << 16);
   }
   // the four block scales, gathered into lane 0

@@ -38,8 +38,31 @@ def _inputs(seed, n, in_f32):
     return bits, bits
 
 
-def _write(oracle_mod, seed, n, fmt, in_f32, num_pages, row_pad=0, page_pad=0, kv_pad=0):
-    host, oracle_in = _inputs(seed, n, in_f32)
+def _edge_inputs(seed, n, in_f32):
+    """Rows built to stress the quotient x / scale: negative zeros inside live blocks, values
+    at the block maximum and at exact multiples of the block scale (ties after scaling), tiny
+    values down to the bf16 subnormals beside large ones, and exponents over 60 decades."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, 576)).astype(np.float32)
+    x *= (10.0 ** rng.uniform(-30, 30, size=(n, 1))).astype(np.float32)
+    x[::3, 5:40] = -0.0
+    x[1::3, :128] *= np.float32(1e-36)
+    x[1::3, 7] = np.float32(9.2e-41)                          # a bf16 subnormal
+    x[2::3, 130:250] = np.float32(-0.0)
+    amax = np.abs(x[:, 256:384]).max(axis=1, keepdims=True)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    k = rng.integers(-448, 449, size=(n, 128)).astype(np.float32)
+    x[:, 256:384] = (k * scale).astype(np.float32)            # multiples of the block scale
+    x[:, 384] = amax[:, 0]                                    # the maximum itself
+    x[:, 385] = -amax[:, 0]
+    if in_f32:
+        return x, x
+    bits = synth.f32_to_bf16_bits(x)
+    return bits, bits
+
+
+def _write(oracle_mod, seed, n, fmt, in_f32, num_pages, row_pad=0, page_pad=0, kv_pad=0, edge=False):
+    host, oracle_in = (_edge_inputs if edge else _inputs)(seed, n, in_f32)
     row_bytes = 1152 if fmt == 0 else 656
     row_stride = row_bytes + row_pad
     page_stride = 64 * row_stride + page_pad
@@ -75,6 +98,12 @@ def _write(oracle_mod, seed, n, fmt, in_f32, num_pages, row_pad=0, page_pad=0, k
 def test_quantize_kv_bit_exact_small(oracle_mod, fmt, in_f32):
     got, expect = _write(oracle_mod, 700 + 2 * fmt + in_f32, 1000, fmt, in_f32, num_pages=40, row_pad=32,
                          page_pad=48, kv_pad=8 if in_f32 else 16)
+    assert np.array_equal(got, expect)
+
+
+@pytest.mark.parametrize("in_f32", [False, True])
+def test_quantize_kv_bit_exact_edge_values(oracle_mod, in_f32):
+    got, expect = _write(oracle_mod, 800 + in_f32, 3000, 1, in_f32, num_pages=60, edge=True)
     assert np.array_equal(got, expect)
 
 

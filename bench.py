@@ -207,23 +207,31 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
 
 
-def kernel_source_hash():
+# Source files that define or launch each workload's dominant kernel: a traffic figure stays
+# valid while these are unchanged.
+KERNEL_SOURCES = {
+    "attention": ("smla_kernels.cu", "smla_ptx.cuh", "smla_internal.h", "smla_api.cu"),
+    "quantize_kv": ("smla_quant.cu", "smla_ptx.cuh", "smla_internal.h"),
+}
+
+
+def kernel_source_hash(workload_key="decode"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_top_mla_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES["quantize_kv" if workload_key == "quantize_kv" else "attention"]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload_key):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
-    when the kernel sources changed since that capture."""
+    when that kernel's sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     d = json.load(open(path))
     e = d.get(workload_key)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(workload_key):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -58,9 +58,9 @@ def test_prefill_roofline_is_tensor_flops():
 
 def test_traffic_only_for_the_captured_source(monkeypatch):
     d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: d["decode"]["kernel_source_hash"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda key="decode": d["decode"]["kernel_source_hash"])
     assert bench.ncu_traffic("decode") == d["decode"]["dram_bytes_per_launch"]
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda key="decode": "0" * 16)
     assert bench.ncu_traffic("decode") is None
 
 

@@ -394,10 +394,11 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
     # step's inputs (q, indices, token_seq, seq_lens, block table, sink) sit packed in one pinned
     # host buffer and are uploaded with one copy into one device buffer the call's tensors view;
     # O and LSE come back with one copy. The copies run on their own streams so they overlap the
-    # kernels of neighbouring steps, as in a serving loop: uploads of step s on the input stream,
-    # the forward on the compute stream once they have landed, the download of step s on the
-    # output stream once it is done. Every rotation has its own device buffers, rewritten only
-    # after its previous forward and download completed (events); host output buffers alternate.
+    # kernels of neighbouring steps, as in a serving loop: uploads on the input stream, the
+    # forwards on the compute stream once their inputs have landed, the downloads on the output
+    # stream once the forwards are done (synchronised per group of steps, below). Every rotation
+    # has its own device buffers, rewritten only after its previous forward and download
+    # completed; host output buffers alternate between two groups.
     def packed(parts):
         offs, n = [], 0
         for a in parts:
@@ -446,17 +447,23 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
         d_in.append(dbuf)
         h_in.append(host)
         d_out.append(obuf)
-    h_out2 = [torch.empty(d_out[0].numel(), dtype=torch.uint8).pin_memory() for _ in range(2)]
     h2d = h_in[0].numel()
     d2h = d_out[0].numel()
-    e2e_steps = min(steps, 20)
+    # steps go in groups of G: one event per group orders the group's uploads before its
+    # forwards, the forwards before the group's downloads, and a rotation's reuse after its
+    # previous group; inside a group the forwards follow each other directly, so each call's
+    # kernels launch behind the previous call's without a synchronisation between them
+    nrot = len(e_calls)
+    G = 4 if nrot % 4 == 0 and nrot >= 8 else 1  # single-rotation workloads: a group per step
+    e2e_steps = max(G, (min(steps, 40) // G) * G)
+    ngroups = e2e_steps // G
+    h_out = [torch.empty(d_out[0].numel(), dtype=torch.uint8).pin_memory() for _ in range(2 * G)]
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
-    nrot = len(e_calls)
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    up_done = [ev() for _ in range(e2e_steps)]
-    fwd_done = [ev() for _ in range(e2e_steps)]
-    down_done = [ev() for _ in range(e2e_steps)]
+    up_done = [ev() for _ in range(ngroups)]
+    fwd_done = [ev() for _ in range(ngroups)]
+    down_done = [ev() for _ in range(ngroups)]
     for c in e_calls[:1]:  # one untimed pass through this path
         d_in[0].copy_(h_in[0])
         binding.forward(c, stream)
@@ -467,24 +474,29 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
-    for s in range(e2e_steps):
-        r = s % nrot
+    gpr = nrot // G  # groups per rotation cycle
+    for g in range(ngroups):
         with torch.cuda.stream(s_in):
-            if s >= nrot:
-                s_in.wait_event(fwd_done[s - nrot])  # the rotation's previous forward read its inputs
-            d_in[r].copy_(h_in[r], non_blocking=True)
-            up_done[s].record(s_in)
-        stream.wait_event(up_done[s])
-        if s >= nrot:
-            stream.wait_event(down_done[s - nrot])  # the rotation's previous outputs were read back
-        binding.forward(e_calls[r], stream)
-        fwd_done[s].record(stream)
+            if g >= gpr:
+                s_in.wait_event(fwd_done[g - gpr])  # these rotations' previous forwards read their inputs
+            for k in range(G):
+                r = (g * G + k) % nrot
+                d_in[r].copy_(h_in[r], non_blocking=True)
+            up_done[g].record(s_in)
+        stream.wait_event(up_done[g])
+        if g >= gpr:
+            stream.wait_event(down_done[g - gpr])  # these rotations' previous outputs were read back
+        for k in range(G):
+            binding.forward(e_calls[(g * G + k) % nrot], stream)
+        fwd_done[g].record(stream)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(fwd_done[s])
-            h_out2[s & 1].copy_(d_out[r], non_blocking=True)
-            down_done[s].record(s_out)
-    stream.wait_event(down_done[e2e_steps - 1])
-    stream.wait_event(up_done[e2e_steps - 1])
+            s_out.wait_event(fwd_done[g])
+            for k in range(G):
+                r = (g * G + k) % nrot
+                h_out[(g & 1) * G + k].copy_(d_out[r], non_blocking=True)
+            down_done[g].record(s_out)
+    stream.wait_event(down_done[ngroups - 1])
+    stream.wait_event(up_done[ngroups - 1])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)

@@ -325,7 +325,7 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
     # timed region. The dominant kernel is timed with events on every KSAMPLE-th step only: an
     # event recorded between two kernels stops the second from launching programmatically (early)
     # behind the first, so the other steps run as a plain stream of calls.
-    ksample = 4
+    ksample = 8
     sampled = [s for s in range(steps) if s % ksample == 0]
     kev = {s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in sampled}
     for a, b in kev.values():  # torch creates CUDA events lazily: record once so the handles exist

@@ -1245,17 +1245,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Split-K combine, one CTA per (token, 32-head chunk, half of the 512 channels). Each thread
-// owns an 8-head subgroup and 4 channels of the half; it issues the loads of its first four
+// Split-K combine, one CTA per (token, 32-head chunk, part of the 512 channels). Each thread
+// owns an 8-head subgroup and 4 (2) channels of the half (quarter); it issues the loads of its first four
 // partial slots before anything else, so they are in flight while threads 0..31 merge the
 // heads' partial base-2 LSEs into the final LSE, the sink factor and the per-slot weights
 // 2^(lse_s - lse) (shared memory). The weighted sums are transposed through shared memory and
 // written as bf16 O with 16-byte stores.
 constexpr int kCombineThreads = 256;
 constexpr int kCombineHeads = 32;
-constexpr int kCombineHalves = 2;
-constexpr int kCombineCh = kDv / kCombineHalves;  // channels per CTA: 256
-constexpr int kCombineSlots = 4;                  // partial slots loaded per round
+constexpr int kCombineSlots = 4;  // partial slots loaded per round
+// The 512 channels are split over kParts CTAs: 2 when T x head chunks already fill the GPU, 4
+// when they leave SMs idle (more CTAs, half the loads per thread, for small T).
+constexpr int kCombineFewCtas = 128;
 
 __device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int& c0, int& ns) {
   const long long item = static_cast<long long>(t) * a.groups + h / a.heads_per_group;
@@ -1264,7 +1265,9 @@ __device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int&
   ns = static_cast<int>(split_owner(x0 + a.tiles_per_item - 1, a.total_tiles, a.nctas)) - c0 + 1;
 }
 
+template <int kParts>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int kCombineCh = kDv / kParts;  // channels per CTA
   extern __shared__ float wts[];  // [max_slots][kCombineHeads]
   __shared__ float fac[kCombineHeads];
   __shared__ __align__(16) uint16_t ot[kCombineHeads][kCombineCh];
@@ -1281,7 +1284,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 
   // 16-byte chunk (channel cbase + tid/4 + 64q, heads hbase + 8g .. +7) of every slot's
   // partial block: four consecutive threads read one channel's 64 contiguous bytes
-  constexpr int kChunks = kCombineCh * (kCombineHeads / 8) / kCombineThreads;  // 4
+  constexpr int kChunks = kCombineCh * (kCombineHeads / 8) / kCombineThreads;  // 4 or 2
   constexpr int kChStep = kCombineThreads / 4;
   const int g = tid & 3;
   int ns = 0;  // slots of this thread's 8 heads (heads_per_group is a multiple of 8)
@@ -1407,8 +1410,8 @@ cudaError_t enable_smem(K kernel, int bytes, std::atomic<uint64_t>& done, std::a
 }
 
 // one record for the combine kernel, which every attention instantiation launches
-std::atomic<uint64_t> g_combine_attr_done{0};
-std::atomic<int> g_combine_attr_bytes{0};
+std::atomic<uint64_t> g_combine_attr_done[2] = {};
+std::atomic<int> g_combine_attr_bytes[2] = {};
 
 template <int NH, int F0, int F1>
 cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, cudaEvent_t ev0, cudaEvent_t ev1) {
@@ -1443,17 +1446,21 @@ cudaError_t launch_nh(const AttnArgs& a, const Plan& plan, cudaStream_t stream, 
   if (plan.split) {
     // programmatic dependent launch: the combine grid is scheduled while the attention kernel
     // drains and waits (griddepcontrol.wait) for its results
+    const unsigned chunks = static_cast<unsigned>((a.H + kCombineHeads - 1) / kCombineHeads);
+    const bool few = static_cast<long long>(a.T) * chunks * 2 < kCombineFewCtas;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.T), (a.H + kCombineHeads - 1) / kCombineHeads, kCombineHalves);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.T), chunks, few ? 4 : 2);
     cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(a.max_slots) * kCombineHeads * sizeof(float);
-    e = enable_smem(combine_kernel, static_cast<int>(cfg.dynamicSmemBytes), g_combine_attr_done,
-                    g_combine_attr_bytes, "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)");
+    e = few ? enable_smem(combine_kernel<4>, static_cast<int>(cfg.dynamicSmemBytes), g_combine_attr_done[1],
+                          g_combine_attr_bytes[1], "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)")
+            : enable_smem(combine_kernel<2>, static_cast<int>(cfg.dynamicSmemBytes), g_combine_attr_done[0],
+                          g_combine_attr_bytes[0], "cudaFuncSetAttribute(combine_kernel, max dynamic shared memory)");
     if (e != cudaSuccess) return e;
     cfg.stream = stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
+    e = few ? cudaLaunchKernelEx(&cfg, combine_kernel<4>, a) : cudaLaunchKernelEx(&cfg, combine_kernel<2>, a);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) note_cuda_error(e, "launch of combine_kernel");
   }

@@ -158,13 +158,20 @@ int ntiles_of(const smla_kv_set& s) { return (s.topk + kTile - 1) / kTile; }
 Plan make_plan(const smla_params* p, bool split_k) {
   Plan pl{};
   pl.groups = (p->H + kMaxGroupHeads - 1) / kMaxGroupHeads;
+  const long long sms = sm_count();
+  const int tiles_per_item = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
+  // split-K with little work (small T): two head groups for 33..64 heads when that still fits
+  // one tile per SM, so twice the CTAs each carry half the heads (shorter MMAs, softmax and
+  // epilogue on the latency-bound path; each row is gathered twice, which at this size costs
+  // nothing measurable)
+  if (split_k && pl.groups == 1 && p->H > 32 && static_cast<long long>(p->T) * tiles_per_item * 2 <= sms)
+    pl.groups = 2;
   // a multiple of 8, so every group's first head starts a 16-byte run in the partial layout
   pl.heads_per_group = (((p->H + pl.groups - 1) / pl.groups) + 7) & ~7;
   pl.nh = pl.heads_per_group <= 16 ? 16 : (pl.heads_per_group <= 32 ? 32 : 64);
-  pl.tiles_per_item = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
+  pl.tiles_per_item = tiles_per_item;
   pl.n_items = static_cast<long long>(p->T) * pl.groups;
   pl.total_tiles = pl.n_items * pl.tiles_per_item;
-  const long long sms = sm_count();
   pl.split = split_k ? 1 : 0;
   pl.max_slots = 1;
   if (pl.split) {

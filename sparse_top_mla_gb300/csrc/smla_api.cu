@@ -160,14 +160,19 @@ Plan make_plan(const smla_params* p, bool split_k) {
   pl.groups = (p->H + kMaxGroupHeads - 1) / kMaxGroupHeads;
   const long long sms = sm_count();
   const int tiles_per_item = ntiles_of(p->main) + (p->extra ? ntiles_of(*p->extra) : 0);
-  // split-K with little work (small T): two head groups for 33..64 heads when that still fits
-  // one tile per SM, so twice the CTAs each carry half the heads (shorter MMAs, softmax and
-  // epilogue on the latency-bound path; each row is gathered twice, which at this size costs
-  // nothing measurable)
-  if (split_k && pl.groups == 1 && p->H > 32 && static_cast<long long>(p->T) * tiles_per_item * 2 <= sms)
-    pl.groups = 2;
   // a multiple of 8, so every group's first head starts a 16-byte run in the partial layout
-  pl.heads_per_group = (((p->H + pl.groups - 1) / pl.groups) + 7) & ~7;
+  auto group_heads = [&](int g) { return (((p->H + g - 1) / g) + 7) & ~7; };
+  // split-K with little work (small T): more, smaller head groups (up to four, at least 16
+  // heads each, none empty) while the grid still fits one tile per SM, so more CTAs each carry
+  // fewer heads on their latency-bound path (MMAs, softmax, epilogue); each row is then
+  // gathered once per group, which at this size costs nothing measurable
+  while (split_k && pl.groups < 4) {
+    const int g2 = 2 * pl.groups;
+    const int h2 = group_heads(g2);
+    if (h2 < 16 || (g2 - 1) * h2 >= p->H || static_cast<long long>(p->T) * tiles_per_item * g2 > sms) break;
+    pl.groups = g2;
+  }
+  pl.heads_per_group = group_heads(pl.groups);
   pl.nh = pl.heads_per_group <= 16 ? 16 : (pl.heads_per_group <= 32 ? 32 : 64);
   pl.tiles_per_item = tiles_per_item;
   pl.n_items = static_cast<long long>(p->T) * pl.groups;

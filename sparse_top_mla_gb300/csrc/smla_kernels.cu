@@ -209,12 +209,12 @@ struct Cursor {
   }
 };
 
-// At most two head groups per token (H <= 128, 64 heads per group).
+// Head groups per token: 1, 2 or 4 (a power of two); item = token * groups + group.
 __device__ __forceinline__ uint32_t item_token(const AttnArgs& a, uint32_t item) {
-  return a.groups == 2 ? item >> 1 : item;
+  return item >> (31 - __clz(a.groups));
 }
 __device__ __forceinline__ int item_head0(const AttnArgs& a, uint32_t item) {
-  return a.groups == 2 ? static_cast<int>(item & 1u) * a.heads_per_group : 0;
+  return static_cast<int>(item & static_cast<uint32_t>(a.groups - 1)) * a.heads_per_group;
 }
 
 __device__ __forceinline__ int set_of(const AttnArgs& a, int tile) {

@@ -1,7 +1,7 @@
 """Benchmark: sparse top-k MLA attention on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl smla|reference]
-                    [--workload decode|prefill|large_prefill|tiny] [--no-secondary]
+                    [--workload decode|prefill|large_prefill|tiny|quantize|small_t] [--no-secondary]
 
 The headline step is one smla_forward call (index resolve, gather + FP8 dequant, QK^T,
 softmax with sink, PV, split-K partials, combine) over the decode workload: 64 sequences x
@@ -39,7 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse-MLA prefill TFLOP/s & decode µs/call + GB/s, as % of roofline"
 ROTATIONS = 8
 # about half a second of timed GPU work per workload
-DEFAULT_STEPS = {"decode": 6000, "prefill": 800, "large_prefill": 40, "tiny": 8000, "quantize": 200}
+DEFAULT_STEPS = {"decode": 6000, "prefill": 800, "large_prefill": 40, "tiny": 8000, "quantize": 200, "small_t": 1}
 
 
 def parse():
@@ -50,7 +50,7 @@ def parse():
                          "20 ms clock samples fall inside the timed region)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny", "quantize"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "large_prefill", "tiny", "quantize", "small_t"])
     ap.add_argument("--no-secondary", action="store_true",
                     help="decode only: leave the prefill, large-prefill and cache-writer workloads out of the line")
     ap.add_argument("--tokens", type=int, default=0,
@@ -386,7 +386,7 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
            "ms_per_step": total_ms / steps, "kern_avg_ms": kern_avg_ms, "kern_samples": len(kern_ms),
            "gathered": gathered[0], "flops": flops, "idx_bytes": idx_bytes, "q_bytes": q_bytes,
            "alg_bytes": w0.algorithmic_bytes(), "clocks": clk, "launches": launches_per_step * steps,
-           "peaks": peaks}
+           "peaks": peaks, "probs": probs}
     if not with_e2e:
         return res
 
@@ -652,6 +652,56 @@ def time_quantize(steps, warmup, world, local):
             "clocks": ClockSampler.summarise([], None, None, (before, after)), "gpu_launches": steps}
 
 
+def time_small_t(probs):
+    """Small-T latency on the decode workload's cache and queries: T = 1, 16, 64 query tokens,
+    H = 64, the first 512 of each token's entries (topk = 512, FP8), one call per rotation, through
+    the crossover dispatch. us_per_call: GPU time per call from a CUDA-graph replay of the rotating
+    calls (host submission excluded, best of 5); attention_launch_us: CUDA events recorded on the
+    stream around the attention kernel's launch alone (median of 32 calls): the kernel and its launch
+    latency, without the overlap with the neighbouring calls that the replay has, and without the
+    combine. The kernels' own durations come from a profiler's launch list of --workload small_t."""
+    import statistics
+    import numpy as np
+    import torch
+    from sparse_top_mla_gb300 import binding, calibrate
+    stream = torch.cuda.current_stream()
+    res, launches = {}, 0
+    for T in (1, 16, 64):
+        calls = []
+        for p in probs[:4]:
+            m = p.main
+            main = binding.DeviceSet(m.cache, m.format, m.row_stride, m.page_stride, m.num_pages, m.block_table,
+                                     m.seq_lens, m.indices[:T, :512], 512)
+            calls.append(binding.Call(p.q[:T], p.token_seq[:T], main, p.out[:T], p.lse[:T], None, p.sink,
+                                      np.float32(p.w.sm_scale), None, num_seqs=p.w.num_seqs))
+        need = max(binding.workspace_size(c) for c in calls)
+        ws = torch.empty(need, dtype=torch.uint8, device=probs[0].device) if need else None
+        for c in calls:
+            c.set_workspace(ws)
+        split = T <= binding.decode_max_tokens(64, 512, probs[0].main.format)
+        reps, inner = 5, 4
+        us = calibrate._time_us(binding.forward, calls, stream, reps, inner)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(32)]
+        for a, b in evs:
+            a.record(stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(evs):
+            binding.set_timing_events(a, b)
+            binding.forward(calls[i % len(calls)], stream)
+        binding.set_timing_events(None, None)
+        torch.cuda.synchronize()
+        assert binding.device_error() == 0
+        ker = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+        res[f"T={T}"] = {"us_per_call": round(us, 2), "attention_launch_us": round(ker, 2),
+                         "schedule": "split-K + combine" if split else "whole items"}
+        ncalls = len(calls) * (1 + inner * (1 + reps)) + len(evs)
+        launches += ncalls * (2 if split else 1)
+    res["workload"] = ("decode cache (64 seqs x 16384 ctx, FP8), H=64, first 512 entries of each token "
+                       "(5% -1), sink; 4 rotating query/index sets")
+    return res, launches
+
+
 def secondary_for(kind, r, cpu):
     """The prefill-type workload as a sub-object of the decode line (TFLOP/s headline)."""
     us = r["ms_per_step"] * 1e3
@@ -679,6 +729,23 @@ def main():
     if rank == 0:
         smla_build.build()
     barrier(world)
+    if args.workload == "small_t":
+        import torch
+        from sparse_top_mla_gb300 import binding
+        dev = torch.device(f"cuda:{local}")
+        torch.cuda.set_device(dev)
+        rots, _ = build_workloads("decode")
+        probs = [binding.DeviceProblem(rots[0], device=dev)]
+        probs += [binding.DeviceProblem(w, device=dev, share_caches_with=probs[0]) for w in rots[1:4]]
+        st, n = time_small_t(probs)
+        if rank == 0:
+            line = {"metric": METRIC, "value": st["T=1"]["us_per_call"], "unit": "us/call", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": st["T=1"]["us_per_call"] / 1e3,
+                    "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                    "data": "synthetic", "config": {"workload": "small T (value: T=1): " + st["workload"],
+                                                    "small_t": st}, "gpu_launches": n}
+            print(json.dumps(line), flush=True)
+        return 0
     if args.workload == "quantize":
         qr = time_quantize(args.steps, args.warmup, world, local)
         if rank == 0:
@@ -693,12 +760,15 @@ def main():
     cpu = cpu_baseline_decode() if (rank == 0 and world == 1 and args.workload == "decode") else None
     line = line_for(args.workload, r, args, world, cpu)
     if args.workload == "decode" and not args.no_secondary:
+        line["config"]["small_t"], n_small = time_small_t(r.pop("probs"))
+        line["gpu_launches"] += n_small
         # the prefill half of the metric, in the same line: each workload timed for the same
         # number of steps when --steps is given, else for its own default (about half a second)
         for kind, n_tok in (("prefill", 256), ("large_prefill", 16)):
             steps = args.steps if args.steps_given else DEFAULT_STEPS[kind]
             rr = time_workload(kind, steps, args.warmup, world, rank, local, False, args.tokens)
             cpu_k = cpu_baseline_tokens(kind, n_tok) if (rank == 0 and world == 1) else None
+            rr.pop("probs", None)
             line["config"][kind] = secondary_for(kind, rr, cpu_k)
             line["gpu_launches"] += rr["launches"]
             import torch

@@ -1261,8 +1261,15 @@ constexpr int kCombineFewCtas = 128;
 __device__ __forceinline__ void item_slots(const AttnArgs& a, int t, int h, int& c0, int& ns) {
   const long long item = static_cast<long long>(t) * a.groups + h / a.heads_per_group;
   const long long x0 = item * a.tiles_per_item;
-  c0 = static_cast<int>(split_owner(x0, a.total_tiles, a.nctas));
-  ns = static_cast<int>(split_owner(x0 + a.tiles_per_item - 1, a.total_tiles, a.nctas)) - c0 + 1;
+  const long long x1 = x0 + a.tiles_per_item - 1;
+  if ((a.total_tiles + 1) * a.nctas < (1ll << 32)) {  // 32-bit divisions (every realistic size)
+    const uint32_t tot = static_cast<uint32_t>(a.total_tiles), nc = static_cast<uint32_t>(a.nctas);
+    c0 = static_cast<int>((static_cast<uint32_t>(x0 + 1) * nc - 1u) / tot);
+    ns = static_cast<int>((static_cast<uint32_t>(x1 + 1) * nc - 1u) / tot) - c0 + 1;
+  } else {
+    c0 = static_cast<int>(split_owner(x0, a.total_tiles, a.nctas));
+    ns = static_cast<int>(split_owner(x1, a.total_tiles, a.nctas)) - c0 + 1;
+  }
 }
 
 template <int kParts>
@@ -1315,9 +1322,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       item_slots(a, t, h, c0, nh);
       const float* lp = a.part_lse + static_cast<int64_t>(t) * H + h;
       const int64_t lstride = static_cast<int64_t>(a.T) * H;
-      // the partial LSEs go to shared memory first (all loads in flight together), then the
-      // max, the sum and the weights are computed from there
-      for (int s = 0; s < nh; ++s) wts[s * kCombineHeads + tid] = lp[s * lstride];
+      // the sink and the first slots' partial LSEs are loaded together (one round trip), the
+      // LSEs go to shared memory, and the max, the sum and the weights are computed from there
+      const float sk = a.sink != nullptr ? a.sink[h] : 0.f;
+      float l0[kCombineSlots];
+#pragma unroll
+      for (int s = 0; s < kCombineSlots; ++s) l0[s] = s < nh ? lp[s * lstride] : 0.f;
+      for (int s = kCombineSlots; s < nh; ++s) wts[s * kCombineHeads + tid] = lp[s * lstride];
+#pragma unroll
+      for (int s = 0; s < kCombineSlots; ++s)
+        if (s < nh) wts[s * kCombineHeads + tid] = l0[s];
       float M = -INFINITY;
       for (int s = 0; s < nh; ++s) M = fmaxf(M, wts[s * kCombineHeads + tid]);
       float L2 = -INFINITY;
@@ -1328,7 +1342,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
       }
       for (int s = 0; s < nh; ++s)
         wts[s * kCombineHeads + tid] = L2 == -INFINITY ? 0.f : exp2f(wts[s * kCombineHeads + tid] - L2);
-      if (L2 != -INFINITY) f = a.sink != nullptr ? 1.f / (1.f + exp2f(a.sink[h] * 1.4426950408889634f - L2)) : 1.f;
+      if (L2 != -INFINITY) f = a.sink != nullptr ? 1.f / (1.f + exp2f(sk * 1.4426950408889634f - L2)) : 1.f;
       if (a.lse != nullptr && blockIdx.z == 0)
         a.lse[static_cast<int64_t>(t) * a.lse_stride_t + h] = L2 * 0.6931471805599453f;
     }

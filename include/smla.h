@@ -131,8 +131,8 @@ smla_status smla_prefill(const smla_params* p, smla_stream_t stream);
  * rows, KV-bandwidth-bound; flashinfer PR "explain ..." merged body: decode split-K.) */
 smla_status smla_decode(const smla_params* p, smla_stream_t stream);
 
-/* smla_decode without a caller-provided workspace. The paper has no counterpart: this entry
- * point exists for callers that cannot allocate device memory themselves (a plugin behind a
+/* smla_decode without a caller-provided workspace. None of the cited sources has a
+ * counterpart: this entry point exists for callers that cannot allocate device memory themselves (a plugin behind a
  * fixed C interface that passes only the problem tensors, or a runtime whose device memory
  * is wholly owned by its own pool). It ignores p->workspace / p->workspace_bytes and keeps
  * the split-K partials in a 32 MiB array inside the library, which every GPU that loads

@@ -1246,8 +1246,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const __grid_co
 }
 
 // Split-K combine, one CTA per (token, 32-head chunk, part of the 512 channels). Each thread
-// owns an 8-head subgroup and 4 (2) channels of the half (quarter); it issues the loads of its first four
-// partial slots before anything else, so they are in flight while threads 0..31 merge the
+// owns an 8-head subgroup and 4 channels of a 256-channel part (2 of a 128-channel part); it
+// issues the loads of its first four partial slots before anything else, so they are in
+// flight while threads 0..31 merge the
 // heads' partial base-2 LSEs into the final LSE, the sink factor and the per-slot weights
 // 2^(lse_s - lse) (shared memory). The weighted sums are transposed through shared memory and
 // written as bf16 O with 16-byte stores.

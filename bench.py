@@ -97,6 +97,15 @@ def max_over_ranks(x, world):
 
 
 # ----------------------------------------------------------------------------- workloads
+def workload_label(kind, T=0):
+    """The workload's name in `config.workload`, the same for both arms (T: query tokens timed)."""
+    return {"decode": "decode fp8: 64 seqs x 16384 ctx (688 MB cache), T=64, H=64, topk=2048 (5% -1), sink",
+            "prefill": f"prefill bf16: 1 seq x 32768 ctx, T={T or 4096}, H=32, topk=512 causal, sink",
+            "tiny": "tiny bf16: 1 seq x 256 ctx, T=4, H=16, topk=128, no sink",
+            "large_prefill": (f"large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T={T or 8192}, H=128, "
+                              "topk=2048 causal + 128-token window, sink")}[kind]
+
+
 def build_workloads(kind, tokens=0):
     from sparse_top_mla_gb300 import synth
     T = tokens if tokens > 0 else None
@@ -108,15 +117,14 @@ def build_workloads(kind, tokens=0):
             idx = synth.mask_random(rng, synth.distinct_indices(rng, np.full(base.T, 16383), 2048), 0.05)
             q = synth.make_q(rng, base.T, base.H)
             rots.append(synth.replace(base, q=q, main=synth.replace(base.main, indices=idx)))
-        return rots, "decode fp8: 64 seqs x 16384 ctx (688 MB cache), T=64, H=64, topk=2048 (5% -1), sink"
+        return rots, workload_label("decode")
     if kind == "prefill":
         w = synth.config(3, T=T)
-        return [w], f"prefill bf16: 1 seq x 32768 ctx, T={w.T}, H=32, topk=512 causal, sink"
+        return [w], workload_label("prefill", w.T)
     if kind == "tiny":
-        return [synth.config(1)], "tiny bf16: 1 seq x 256 ctx, T=4, H=16, topk=128, no sink"
+        return [synth.config(1)], workload_label("tiny")
     w = synth.config(4, T=T)
-    return [w], (f"large prefill: 1 seq x 65536 ctx fp8 main + bf16 extra, T={w.T}, H=128, "
-                 "topk=2048 causal + 128-token window, sink")
+    return [w], workload_label("large_prefill", w.T)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -289,7 +297,7 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+            "data": "synthetic", "config": {"workload": workload_label(args.workload, args.tokens), "sample": sample},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}

@@ -98,6 +98,17 @@ def load(path: Optional[str] = None):
     return lib
 
 
+def use_library(path: str):
+    """Load the library at `path` (an instrumented build, for instance) and make it the one every
+    call of this module uses, with this GPU model's crossover table."""
+    global _lib
+    lib = load(path)
+    _lib = lib
+    if os.path.exists(CROSSOVER_TABLE):
+        lib.smla_load_crossover(CROSSOVER_TABLE.encode())
+    return lib
+
+
 def status_string(st: int) -> str:
     return load().smla_status_string(st).decode()
 

@@ -690,7 +690,7 @@ def time_small_t(probs):
             c.set_workspace(ws)
         split = T <= binding.decode_max_tokens(64, 512, probs[0].main.format)
         reps, inner = 5, 4
-        us = calibrate._time_us(binding.forward, calls, stream, reps, inner)
+        us = calibrate.graph_time_us(binding.forward, calls, stream, reps, inner)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(32)]
         for a, b in evs:
             a.record(stream)

@@ -60,7 +60,7 @@ def table_json(entries, meta: dict) -> str:
     return head + "".join(",\n" + l for l in lines) + "\n}\n"
 
 
-def _time_us(fn, calls, stream, reps: int, inner: int = 4) -> float:
+def graph_time_us(fn, calls, stream, reps: int, inner: int = 4) -> float:
     """GPU time per call, from a CUDA graph replaying `inner` rounds of the rotating calls (the
     pages' protocol times graph replays, GPU-only): host submission is then not part of the
     number, which matters at small T where a call is a few microseconds of GPU work."""
@@ -135,8 +135,8 @@ def calibrate(formats=(1,), heads=None, topks=None, t_grid=T_GRID, rotations: in
                         calls.append(binding.Call(qs[r][:T], token_seq[:T], main, out[:T], lse[:T], None, sink,
                                                   np.float32(1.0 / math.sqrt(576)), None, num_seqs=pool.num_seqs))
                     ws_for(calls)
-                    dec = _time_us(binding.decode, calls, stream, reps)
-                    pre = _time_us(binding.prefill, calls, stream, reps)
+                    dec = graph_time_us(binding.decode, calls, stream, reps)
+                    pre = graph_time_us(binding.prefill, calls, stream, reps)
                     pts.append((T, dec, pre))
                 mt = crossover(pts, ratio)
                 entries.append((H, k, fmt, mt))

@@ -333,8 +333,9 @@ def time_workload(kind, steps, warmup, world, rank, local, with_e2e=True, tokens
     # timed region. The dominant kernel is timed with events on every KSAMPLE-th step only: an
     # event recorded between two kernels stops the second from launching programmatically (early)
     # behind the first, so the other steps run as a plain stream of calls.
-    # every 7th step: coprime with the 8 rotations, so the samples cover every index set
-    ksample = 7
+    # every k-th step, k odd (coprime with the 8 rotations, so the samples cover every index set)
+    # and at least 7; long runs take ~200 samples, so the events perturb few calls
+    ksample = max(7, steps // 200) | 1
     sampled = [s for s in range(steps) if s % ksample == 0]
     kev = {s: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for s in sampled}
     for a, b in kev.values():  # torch creates CUDA events lazily: record once so the handles exist
